@@ -147,12 +147,30 @@ class BlockAllocator:
         return table_row[j] * block_size + position % block_size, num_blocks, cow
 
     def fork(self, table_row, num_blocks):
-        """Share every block of a sequence with a new branch (count + 1 each)."""
-        for b in table_row[:num_blocks]:
-            self.incref(b)
+        """Share every block of a sequence with a new branch (count + 1 each).
+
+        All or nothing: a bad id undoes the increments already made."""
+        done = []
+        try:
+            for b in table_row[:num_blocks]:
+                self.incref(b)
+                done.append(b)
+        except AllocError:
+            for b in done:
+                self.ref[b] -= 1
+            raise
 
     def free_sequence(self, table_row, num_blocks):
-        """Drop a sequence: decref its blocks in table order."""
+        """Drop a sequence: decref its blocks in table order.
+
+        All or nothing: every id is checked (in range, referenced as often as
+        the row names it) before any count changes."""
+        uses = {}
+        for b in table_row[:num_blocks]:
+            self._check_id(b)
+            uses[b] = uses.get(b, 0) + 1
+            if self.ref[b] < uses[b]:
+                raise AllocError("INVALID", f"block {b} over-released")
         for b in table_row[:num_blocks]:
             self.decref(b)
 
