@@ -1,0 +1,483 @@
+"""Benchmark of the paged decode hot path on one GB300 (or N independent replicas).
+
+One step = the whole hot path over one batch of the workload: the KV append
+of the step's new tokens (slot scatter kernel) and single-query paged decode
+attention (decode kernel + split-context merge kernel).  Inputs are seeded
+and synthetic; the caches are built through the library before timing.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the oracle on the host cores
+
+Prints one JSON line.  ``value`` is decode tokens/s (batch x steps / time)
+with every input resident in HBM; ``e2e`` is the same metric through the
+public API from pinned host buffers, copies included.  Between timed steps
+the caches rotate over replicas whose total size exceeds L2, so each step
+streams its KV from HBM.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn tokens/s and KV HBM GB/s (fraction of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="gqa_bf16")
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--partition", type=int, default=None, help="tokens per partition (default: the workload's)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------ clock sampler
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------- workload set-up
+
+class GpuWorkload:
+    """A workload's caches, block tables and step inputs on the device."""
+
+    def __init__(self, name, device, replicas, partition=None):
+        import torch
+
+        import paged_kv_cache_257_gb300 as pa
+        from synth import workloads as wl
+        self.pa, self.torch = pa, torch
+        self.w = w = wl.make(name)
+        self.device = device
+        self.partition = w.partition_size if partition is None else partition
+        bs = w.block_size
+        self.alloc_tables(wl)
+        ctx = self.ctx_decode
+        # source values of every cached token (in the cache's source type)
+        k_scale = v_scale = 1.0
+        seqs_k, seqs_v = [], []
+        for s in range(w.batch):
+            n = int(w.context_lens[s]) + (1 if w.prefix_len else 0)
+            seqs_k.append(wl.kv_tokens_f32(w, "k", s, 0, n))
+            seqs_v.append(wl.kv_tokens_f32(w, "v", s, 0, n))
+        if w.kv_dtype == "fp8_e4m3":
+            k_scale = float(max(wl.fp8_scale_of(x) for x in seqs_k))
+            v_scale = float(max(wl.fp8_scale_of(x) for x in seqs_v))
+        self.desc = pa.CacheDesc(w.num_blocks, bs, w.n_kv_heads, w.head_dim, w.kv_dtype, k_scale, v_scale)
+        src = w.src_dtype
+        torch_src = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[src]
+
+        def dev(arr_f32):
+            t = torch.from_numpy(np.ascontiguousarray(arr_f32))
+            return t.to(torch_src).to(device) if src != "f32" else t.to(device)
+
+        # fill the caches through the library: slot mapping then append, in chunks
+        seq_ids = np.concatenate([np.full(len(x), s, np.int32) for s, x in enumerate(seqs_k)])
+        pos = np.concatenate([np.arange(len(x), dtype=np.int32) for x in seqs_k])
+        slots = pa.compute_slot_mapping(self.tables_np, seq_ids, pos, bs)
+        self.pools = []
+        for r in range(replicas):
+            kc, vc = self.desc.new_pools(device, fill=0)
+            self.pools.append((kc, vc))
+        chunk = 1 << 16
+        allk = np.concatenate(seqs_k)
+        allv = np.concatenate(seqs_v)
+        for lo in range(0, len(slots), chunk):
+            k = dev(allk[lo:lo + chunk])
+            v = dev(allv[lo:lo + chunk])
+            sl = torch.from_numpy(slots[lo:lo + chunk]).to(device)
+            for kc, vc in self.pools:
+                pa.kv_append(self.desc, k, v, sl, kc, vc)
+        del allk, allv
+        torch.cuda.synchronize()
+        self.kv_tokens = int(np.sum(ctx))
+        self.kv_bytes = self.kv_tokens * 2 * w.n_kv_heads * w.head_dim * w.kv_elem_bytes
+        self.unique_kv_bytes = self.kv_bytes
+        if w.prefix_len:
+            uniq = w.prefix_len + int(np.sum(ctx - w.prefix_len))
+            self.unique_kv_bytes = uniq * 2 * w.n_kv_heads * w.head_dim * w.kv_elem_bytes
+        # step inputs
+        q = wl.cast(wl.queries_f32(w), w.q_dtype)
+        if w.q_dtype == "bf16":
+            self.q = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(device)
+        else:
+            self.q = torch.from_numpy(q).to(device)
+        self.block_tables = torch.from_numpy(self.tables_np).to(device)
+        self.context_lens = torch.from_numpy(ctx.astype(np.int32)).to(device)
+        self.new_k, self.new_v, self.new_slots = self.step_append_inputs(wl, dev)
+        self.workspace = None
+        need = pa.decode_workspace_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], self.partition)
+        if need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=device)
+        self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
+        self.resolved_partition = pa.partition_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1],
+                                                    self.partition)
+
+    def alloc_tables(self, wl):
+        w = self.w
+        if w.block_tables is not None:
+            self.tables_np = w.block_tables
+            self.ctx_decode = w.context_lens.astype(np.int64)
+            self.append_positions = None
+            return
+        # prefix sharing: blocks handed out by the library's allocator; the
+        # prefix blocks are shared by every sequence (reference count = batch)
+        self.allocator = self.pa.BlockAllocator(w.num_blocks, w.alloc_seed)
+        self.tables_np, self.ctx_decode, self.append_slots = wl.build_prefix_tables(w, self.allocator)
+        self.append_positions = w.context_lens.copy()
+
+    def step_append_inputs(self, wl, dev):
+        torch = self.torch
+        w = self.w
+        if w.name == "gqa_bf16":
+            slots = wl.append_slots(w)
+            k, v = wl.append_tokens_f32(w, "k"), wl.append_tokens_f32(w, "v")
+        elif w.prefix_len:
+            slots = np.array(self.append_slots, dtype=np.int64)
+            k = np.stack([wl.kv_tokens_f32(w, "k", s, int(c), int(c) + 1)[0] for s, c in enumerate(w.context_lens)])
+            v = np.stack([wl.kv_tokens_f32(w, "v", s, int(c), int(c) + 1)[0] for s, c in enumerate(w.context_lens)])
+        else:
+            return None, None, None
+        return dev(k), dev(v), torch.from_numpy(np.asarray(slots, dtype=np.int64)).to(self.device)
+
+    def step(self, r, decode_events=None):
+        pa = self.pa
+        kc, vc = self.pools[r % len(self.pools)]
+        n = 0
+        if self.new_k is not None:
+            pa.kv_append(self.desc, self.new_k, self.new_v, self.new_slots, kc, vc)
+            n += 1
+        if decode_events is not None:
+            decode_events[0].record()
+        pa.decode_attention(self.desc, self.q, kc, vc, self.block_tables, self.context_lens, self.w.scale,
+                            partition=self.partition, workspace=self.workspace, out=self.out)
+        if decode_events is not None:
+            decode_events[1].record()
+        return n + 1 + (1 if self.workspace is not None else 0)
+
+
+def time_device(wk, steps, warmup):
+    """Timed region: barrier + synchronize, K steps, synchronize; per-decode events too."""
+    torch = wk.torch
+    for i in range(warmup):
+        wk.step(i)
+    torch.cuda.synchronize()
+    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    start.record()
+    for i in range(steps):
+        launches += wk.step(warmup + i, dec[i])
+    end.record()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in dec]
+    return total_ms, dec_ms, launches
+
+
+def time_e2e(wk, steps, warmup):
+    """The public API from pinned host buffers: H2D of the step inputs, the step, D2H of the output."""
+    torch, pa = wk.torch, wk.pa
+    host = {"q": wk.q.cpu().pin_memory(), "bt": wk.block_tables.cpu().pin_memory(),
+            "ctx": wk.context_lens.cpu().pin_memory()}
+    if wk.new_k is not None:
+        host.update(k=wk.new_k.cpu().pin_memory(), v=wk.new_v.cpu().pin_memory(),
+                    slots=wk.new_slots.cpu().pin_memory())
+    out_host = torch.empty(wk.out.shape, dtype=wk.out.dtype).pin_memory()
+    dev = {k: torch.empty_like(v, device=wk.device) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one(r):
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        kc, vc = wk.pools[r % len(wk.pools)]
+        if "k" in dev:
+            pa.kv_append(wk.desc, dev["k"], dev["v"], dev["slots"], kc, vc)
+        pa.decode_attention(wk.desc, dev["q"], kc, vc, dev["bt"], dev["ctx"], wk.w.scale,
+                            partition=wk.partition, workspace=wk.workspace, out=wk.out)
+        out_host.copy_(wk.out, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        one(warmup + i)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end), h2d, d2h
+
+
+# -------------------------------------------------------------- oracle arm
+
+_ORACLE_SETUP = {}
+
+
+def oracle_setup(w_name):
+    """The oracle's own paged cache for a sample of the workload's sequences.
+
+    Small workloads keep every sequence; long ones keep sequence 0 (same
+    shapes, same block ids).  Built once per process, outside any timing."""
+    if w_name in _ORACLE_SETUP:
+        return _ORACLE_SETUP[w_name]
+    from oracle import allocator as oalloc
+    from oracle import cache as ocache
+    from synth import workloads as wl
+    w = wl.make(w_name)
+    if w.block_tables is None:
+        tables, ctx, new_slots = wl.build_prefix_tables(w, oalloc.BlockAllocator(w.num_blocks, w.alloc_seed))
+    else:
+        tables, ctx, new_slots = w.block_tables, w.context_lens.astype(np.int64), None
+    seqs = list(range(w.batch)) if int(np.sum(ctx)) <= 200_000 else [0]
+    kp = ocache.new_pool(w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim, w.kv_dtype)
+    vp = ocache.new_pool(w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim, w.kv_dtype)
+    scales = (1.0, 1.0)
+    vals = {s: (wl.kv_tokens_f32(w, "k", s, 0, int(ctx[s])), wl.kv_tokens_f32(w, "v", s, 0, int(ctx[s])))
+            for s in seqs}
+    if w.kv_dtype == "fp8_e4m3":
+        scales = (float(wl.fp8_scale_of(np.concatenate([vals[s][0].ravel() for s in seqs]))),
+                  float(wl.fp8_scale_of(np.concatenate([vals[s][1].ravel() for s in seqs]))))
+    for s in seqs:
+        n = int(ctx[s])
+        slots = ocache.slot_mapping(tables, [s] * n, range(n), w.block_size)
+        ocache.kv_append(kp, vp, wl.cast(vals[s][0], w.src_dtype), wl.cast(vals[s][1], w.src_dtype), slots,
+                         w.src_dtype, w.kv_dtype, *scales)
+    q = wl.cast(wl.queries_f32(w), w.q_dtype)[seqs]
+    _ORACLE_SETUP[w_name] = (w, seqs, q, kp, vp, tables[seqs], ctx[seqs], scales)
+    return _ORACLE_SETUP[w_name]
+
+
+def oracle_step_sample(w_name, budget_s):
+    """Time the oracle's paged decode attention on the host for about ``budget_s``.
+
+    Returns (decode tokens per second, sequence-steps run, seconds, sample text)."""
+    from oracle import attention as oatt  # test infrastructure: the CPU baseline leg only
+    w, seqs, q, kp, vp, tables, ctx, (ks, vs) = oracle_setup(w_name)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        oatt.decode_attention_paged(q, kp, vp, tables, ctx, w.scale, w.kv_dtype, ks, vs, q_dtype=w.q_dtype)
+        done += len(seqs)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"oracle decode_attention_paged (numpy, float64) over {len(seqs)} of {w.batch} sequences of "
+              f"{w_name} (their block tables and context lengths), {done} sequence-steps in {dt:.1f} s")
+    return done / dt, done, dt, sample
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------- distributed
+
+_dist = None
+
+
+def barrier():
+    if _dist is not None:
+        _dist.barrier()
+
+
+def max_over_ranks(x):
+    if _dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    _dist.all_reduce(t, op=_dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    global _dist
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        _dist = dist
+    import torch
+    from paged_kv_cache_257_gb300 import build
+    build.build()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    from synth import workloads as wl
+    w = wl.make(args.workload)
+    # enough replicas of the caches that their total exceeds L2 several times
+    per = w.num_blocks * w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes * 2
+    replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
+    wk = GpuWorkload(args.workload, device, replicas, args.partition)
+    with ClockSampler(local) as clk:
+        total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup)
+    e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
+    total_ms = max_over_ranks(total_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    value = w.batch * args.steps * world / (total_ms / 1e3)
+    e2e_value = w.batch * args.steps * world / (e2e_ms / 1e3)
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    peak, peak_src = measured_peak()
+    achieved = wk.kv_bytes / dec_avg_s / 1e9
+    step_s = total_ms / 1e3 / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "kv_dtype": w.kv_dtype, "q_dtype": w.q_dtype, "kv_tokens": wk.kv_tokens,
+                   "partition_size": wk.resolved_partition, "append_tokens": w.append_tokens,
+                   "l2": f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)",
+                   "parallelism": f"replicas x{world}"},
+        "kv_tokens_per_s": wk.kv_tokens * world / step_s,
+        "kv_gbs": wk.kv_bytes * world / step_s / 1e9,
+        "decode_kernel_us": dec_avg_s * 1e6,
+        "roofline": {"bound": "hbm", "kernel": "paged decode (decode + split merge)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if wk.unique_kv_bytes != wk.kv_bytes:
+        line["unique_kv_gbs"] = wk.unique_kv_bytes * world / step_s / 1e9
+    if rank == 0 and not args.no_cpu_baseline:
+        v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if _dist is not None:
+        _dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args):
+    """The oracle as the reference arm: K timed steps, each a bounded sample of the workload."""
+    from synth import workloads as wl
+    w = wl.make(args.workload)
+    per_step = max(1.0, min(10.0, 60.0 / max(1, args.steps)))
+    for _ in range(args.warmup):
+        oracle_step_sample(args.workload, 0.0)
+    t0 = time.perf_counter()
+    total = 0
+    sample = ""
+    for _ in range(args.steps):
+        _, done, _, sample = oracle_step_sample(args.workload, per_step)
+        total += done
+    dt = time.perf_counter() - t0
+    value = total / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "batch": w.batch, "n_q_heads": w.n_q_heads,
+                       "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                       "kv_dtype": w.kv_dtype, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,276 @@
+"""Thin Python binding over the C ABI: argument marshalling only.
+
+Every step of the hot path runs in the library's CUDA kernels; torch is used
+here for device memory (tensors the library reads and writes) and for the
+current CUDA stream.  Names follow the C ABI (``pa_kv_append`` ->
+``kv_append`` and so on).
+"""
+
+import ctypes
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import _native
+from ._native import DTYPE, NativeError, check, lib
+
+TORCH_STORAGE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}
+_FROM_TORCH = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+@dataclasses.dataclass
+class CacheDesc:
+    """One layer's paged KV cache: pools ``[num_blocks, num_kv_heads, block_size, head_dim]``."""
+
+    num_blocks: int
+    block_size: int
+    num_kv_heads: int
+    head_dim: int
+    kv_dtype: str = "bf16"
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    def c(self):
+        return _native.CacheDescC(self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim,
+                                  DTYPE[self.kv_dtype], self.k_scale, self.v_scale)
+
+    @property
+    def pool_shape(self):
+        return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+    def new_pools(self, device="cuda", fill=None):
+        """Allocate the K and V pools (torch, device memory); optionally fill raw bytes."""
+        k = torch.empty(self.pool_shape, dtype=TORCH_STORAGE[self.kv_dtype], device=device)
+        v = torch.empty_like(k)
+        if fill is not None:
+            k.view(torch.uint8).fill_(fill)
+            v.view(torch.uint8).fill_(fill)
+        return k, v
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_of(t, what):
+    if t.dtype not in _FROM_TORCH:
+        raise TypeError(f"{what}: unsupported dtype {t.dtype}")
+    return _FROM_TORCH[t.dtype]
+
+
+def _need(t, what, dtype=None, cuda=True):
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------------ info
+
+def version():
+    return lib().pa_version().decode()
+
+
+def dtype_size(dtype):
+    return int(lib().pa_dtype_size(DTYPE[dtype]))
+
+
+def kv_bytes_per_token(n_layers, n_kv_heads, head_dim, dtype):
+    return int(lib().pa_kv_bytes_per_token(n_layers, n_kv_heads, head_dim, DTYPE[dtype]))
+
+
+def compute_slot_mapping(block_tables, seq_ids, positions, block_size):
+    """int64 slots of (sequence, position) pairs from host block tables (numpy)."""
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sid = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    out = np.empty(len(sid), dtype=np.int64)
+    st = lib().pa_compute_slot_mapping(bt.ctypes.data, bt.shape[0], bt.shape[1], block_size, sid.ctypes.data,
+                                      pos.ctypes.data, len(sid), out.ctypes.data)
+    check("pa_compute_slot_mapping", st)
+    return out
+
+
+# ---------------------------------------------------------- device calls
+
+def kv_append(desc, k, v, slot_mapping, k_cache, v_cache, status=None, stream=None):
+    """Write new tokens' K/V rows ``[T, Hkv, D]`` into their slots (``pa_kv_append``)."""
+    for t, n in ((k, "k"), (v, "v"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n)
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    src = _dtype_of(k, "k")
+    if v.dtype != k.dtype:
+        raise TypeError("k and v must share a dtype")
+    c = desc.c()
+    st = lib().pa_kv_append(ctypes.byref(c), _ptr(k), _ptr(v), DTYPE[src], _ptr(slot_mapping),
+                            slot_mapping.numel(), _ptr(k_cache), _ptr(v_cache), _ptr(status), _stream(stream))
+    check("pa_kv_append", st)
+
+
+def copy_blocks(desc, k_cache, v_cache, src_blocks, dst_blocks, status=None, stream=None):
+    """Copy whole physical blocks src -> dst in both pools (``pa_copy_blocks``)."""
+    _need(src_blocks, "src_blocks", torch.int32)
+    _need(dst_blocks, "dst_blocks", torch.int32)
+    c = desc.c()
+    st = lib().pa_copy_blocks(ctypes.byref(c), _ptr(k_cache), _ptr(v_cache), _ptr(src_blocks), _ptr(dst_blocks),
+                              src_blocks.numel(), _ptr(status), _stream(stream))
+    check("pa_copy_blocks", st)
+
+
+def partition_size(desc, batch, num_q_heads, max_blocks_per_seq, requested=0):
+    c = desc.c()
+    return int(lib().pa_decode_partition_size(ctypes.byref(c), batch, num_q_heads, max_blocks_per_seq, requested))
+
+
+def decode_workspace_size(desc, batch, num_q_heads, max_blocks_per_seq, partition=0):
+    c = desc.c()
+    return int(lib().pa_decode_workspace_size(ctypes.byref(c), batch, num_q_heads, max_blocks_per_seq, partition))
+
+
+def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scale, partition=0, workspace=None,
+                     out=None, out_dtype=None, status=None, stream=None):
+    """Single-query paged decode attention (``pa_decode_attention``); returns ``out``.
+
+    ``q`` is ``[batch, num_q_heads, head_dim]``; ``block_tables`` int32
+    ``[batch, max_blocks]``; ``context_lens`` int32 ``[batch]``.  ``out`` and
+    the split-context ``workspace`` are allocated with torch when not given.
+    """
+    _need(q, "q")
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    batch, hq, d = q.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        od = out_dtype or "f32"
+        out = torch.empty((batch, hq, d), dtype=TORCH_STORAGE[od], device=q.device)
+    _need(out, "out")
+    od = _dtype_of(out, "out")
+    need = decode_workspace_size(desc, batch, hq, max_blocks, partition)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    c = desc.c()
+    st = lib().pa_decode_attention(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
+                                   float(scale), partition, _ptr(workspace) if need else None,
+                                   need if need else 0, _ptr(out), DTYPE[od], _ptr(status), _stream(stream))
+    check("pa_decode_attention", st)
+    return out
+
+
+def new_status(device="cuda"):
+    """A zeroed device status word for the ``status=`` arguments."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_device_status(status, reset=True, stream=None):
+    """Flags raised on the device since the word was last cleared (synchronises the stream)."""
+    flags = ctypes.c_int32(0)
+    st = lib().pa_read_device_status(_ptr(status), ctypes.byref(flags), 1 if reset else 0, _stream(stream))
+    if st not in (0, 6):
+        check("pa_read_device_status", st)
+    return int(flags.value)
+
+
+# ------------------------------------------------------------- allocator
+
+_ALLOC_STATUS = {2: "OOM", 1: "INVALID", 3: "RANGE"}
+
+
+class AllocError(Exception):
+    """Allocator failure; ``status`` is "OOM", "INVALID" or "RANGE"."""
+
+    def __init__(self, status, fn):
+        super().__init__(f"{fn}: {status}")
+        self.status = status
+
+
+def _alloc_check(fn, st):
+    if st != 0:
+        if st in _ALLOC_STATUS:
+            raise AllocError(_ALLOC_STATUS[st], fn)
+        check(fn, st)
+
+
+class BlockAllocator:
+    """The library's host block allocator (``pa_alloc_*``), same methods as the model."""
+
+    def __init__(self, num_blocks, seed=0):
+        h = ctypes.c_void_p()
+        _alloc_check("pa_alloc_create", lib().pa_alloc_create(num_blocks, seed, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib().pa_alloc_destroy(h)
+            self._h = None
+
+    def alloc(self):
+        b = ctypes.c_int32()
+        _alloc_check("pa_alloc_block", lib().pa_alloc_block(self._h, ctypes.byref(b)))
+        return b.value
+
+    def incref(self, b):
+        _alloc_check("pa_alloc_incref", lib().pa_alloc_incref(self._h, b))
+
+    def decref(self, b):
+        _alloc_check("pa_alloc_decref", lib().pa_alloc_decref(self._h, b))
+
+    def cow(self, b):
+        nb, copied = ctypes.c_int32(), ctypes.c_int32()
+        _alloc_check("pa_alloc_cow", lib().pa_alloc_cow(self._h, b, ctypes.byref(nb), ctypes.byref(copied)))
+        return nb.value, bool(copied.value)
+
+    def append_slot(self, table_row, num_blocks, position, block_size):
+        """Slot for logical token ``position``; updates ``table_row`` (a list) in place.
+
+        Returns ``(slot, num_blocks, cow)`` with ``cow`` = ``(src, dst)`` or None."""
+        arr = (ctypes.c_int32 * len(table_row))(*table_row)
+        n = ctypes.c_int32(num_blocks)
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        st = lib().pa_alloc_append_slot(self._h, arr, len(table_row), ctypes.byref(n), position, block_size,
+                                        ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst))
+        _alloc_check("pa_alloc_append_slot", st)
+        table_row[:] = list(arr)
+        return slot.value, n.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def fork(self, table_row, num_blocks):
+        arr = np.ascontiguousarray(table_row[:num_blocks], dtype=np.int32)
+        _alloc_check("pa_alloc_fork", lib().pa_alloc_fork(self._h, arr.ctypes.data, num_blocks))
+
+    def free_sequence(self, table_row, num_blocks):
+        arr = np.ascontiguousarray(table_row[:num_blocks], dtype=np.int32)
+        _alloc_check("pa_alloc_free_sequence", lib().pa_alloc_free_sequence(self._h, arr.ctypes.data, num_blocks))
+
+    @property
+    def free_count(self):
+        return int(lib().pa_alloc_free_count(self._h))
+
+    def refcount(self, b):
+        return int(lib().pa_alloc_refcount(self._h, b))
+
+    @property
+    def ref(self):
+        return self.dump()[1]
+
+    def dump(self):
+        free = np.empty(self.num_blocks, dtype=np.int32)
+        ref = np.empty(self.num_blocks, dtype=np.int32)
+        nf = ctypes.c_int32()
+        _alloc_check("pa_alloc_dump", lib().pa_alloc_dump(self._h, free.ctypes.data, ctypes.byref(nf),
+                                                           ref.ctypes.data))
+        return [int(x) for x in free[:nf.value]], [int(x) for x in ref]
+
+
+__all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
+           "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size",
+           "decode_workspace_size", "decode_attention", "new_status", "read_device_status"]

@@ -1,0 +1,209 @@
+// Device helpers shared by the kernels: element conversions, bounded
+// mbarrier waits, TMA tile loads and the warp-level tensor-core primitives.
+// Everything here is sm_103a inline PTX or CUDA intrinsics.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// ------------------------------------------------------------- status flags
+
+__device__ __forceinline__ void raise_flag(int32_t* status, int32_t bit) {
+    if (status != nullptr) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------- element access
+
+template <pa_dtype T> struct Elem;
+template <> struct Elem<PA_F32>      { using type = float;          static constexpr int bytes = 4; };
+template <> struct Elem<PA_F16>      { using type = __half;         static constexpr int bytes = 2; };
+template <> struct Elem<PA_BF16>     { using type = __nv_bfloat16;  static constexpr int bytes = 2; };
+template <> struct Elem<PA_FP8_E4M3> { using type = uint8_t;        static constexpr int bytes = 1; };
+
+// Value of one stored element as float (FP8 codes without their scale).
+template <pa_dtype T> __device__ __forceinline__ float to_float(const void* p, int64_t i);
+template <> __device__ __forceinline__ float to_float<PA_F32>(const void* p, int64_t i) {
+    return static_cast<const float*>(p)[i];
+}
+template <> __device__ __forceinline__ float to_float<PA_F16>(const void* p, int64_t i) {
+    return __half2float(static_cast<const __half*>(p)[i]);
+}
+template <> __device__ __forceinline__ float to_float<PA_BF16>(const void* p, int64_t i) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+template <> __device__ __forceinline__ float to_float<PA_FP8_E4M3>(const void* p, int64_t i) {
+    __nv_fp8_e4m3 v;
+    v.__x = static_cast<const uint8_t*>(p)[i];
+    return static_cast<float>(v);
+}
+
+// Store a float as an output element (round to nearest even for 16-bit types).
+__device__ __forceinline__ void store_out(void* p, int64_t i, float x, pa_dtype t) {
+    if (t == PA_F32) static_cast<float*>(p)[i] = x;
+    else if (t == PA_F16) static_cast<__half*>(p)[i] = __float2half_rn(x);
+    else static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+}
+
+// ----------------------------------------------------------- fast math
+
+// 2^x by the hardware ex2 instruction (ex2(-inf) = +0).
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// -------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longest time any on-chip wait may take before the kernel gives up.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Wait for the phase of `bar` with parity `parity` to complete; false if the
+// time limit ran out first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------- TMA
+
+// L2 policy for data read exactly once (the KV stream).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled TMA load of the box at (x, y) of `tmap` into shared memory at
+// `dst`, completing `bytes` of transaction on barrier `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tmap, uint32_t bar,
+                                            int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// ------------------------------------------------ warp tensor-core pieces
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// D = A * B + D, m16n8k16, fp32 accumulate; A/B bf16 or f16 per `IS_BF16`.
+template <bool IS_BF16>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (IS_BF16) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row pair per thread.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Two E4M3 codes (low byte -> low half) to two exact float16 values.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_in_low16) {
+    uint32_t y;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+        : "=r"(y)
+        : "r"(two_codes_in_low16));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t y, uint32_t sel) {
+    return __byte_perm(x, y, sel);
+}
+
+// Pack two floats into a 16-bit pair: `lo` in the low half.
+template <bool IS_BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (IS_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+}  // namespace pa

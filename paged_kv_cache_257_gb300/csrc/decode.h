@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI entry points and the decode kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Everything a decode launch needs, already validated on the host.
+struct DecodeArgs {
+    const void* q;                // [batch][num_q_heads][head_dim] of q_dtype
+    const void* k_cache;          // [num_blocks][num_kv_heads][block_size][head_dim]
+    const void* v_cache;
+    const int32_t* block_tables;  // [batch][max_blocks]
+    const int32_t* context_lens;  // [batch]
+    void* out;                    // [batch][num_q_heads][head_dim] of out_dtype
+    float* part_o;                // [batch][num_q_heads][max_parts][head_dim] (split only)
+    float* part_ml;               // [batch][num_q_heads][max_parts][2]: (max, sum) in log2 units
+    int32_t* status;              // device status word or null
+    int32_t batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks;
+    int32_t group;                // num_q_heads / num_kv_heads
+    int32_t partition_size;       // tokens per partition
+    int32_t max_parts;            // ceil(max_blocks * block_size / partition_size)
+    pa_dtype q_dtype, kv_dtype, out_dtype;
+    float scale;                  // softmax scale
+    float k_scale, v_scale;       // FP8 dequantisation scales (1 otherwise)
+};
+
+// Query heads one CTA serves (a KV head's group is split into chunks of this).
+constexpr int kHeadsPerCta = 8;
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Host check of a cache descriptor shared by every entry point.
+pa_status check_cache_desc(const pa_cache_desc* c);
+
+// Tensor-core kernel: 16-bit or FP8 cache, head_dim 128, 16-bit queries.
+bool mma_path_supported(const DecodeArgs& a);
+pa_status launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
+
+// CUDA-core kernel: every supported combination.
+pa_status launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);
+
+// Log-sum-exp merge of the partitions of split sequences.
+pa_status launch_decode_reduce(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace pa

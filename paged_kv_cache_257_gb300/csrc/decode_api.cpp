@@ -1,0 +1,129 @@
+// Entry points of decode attention: argument checks, partition choice,
+// workspace layout and kernel dispatch.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "decode.h"
+#include "pagedattn.h"
+
+namespace pa {
+namespace {
+
+constexpr int kMaxParts = 32768;
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+// Tokens per partition must be a multiple of the 16-token chunk and of the block size.
+int32_t partition_unit(int32_t block_size) { return std::max(16, block_size); }
+
+// Auto choice: the largest partition (fewer partials to merge) that still
+// gives a few waves of CTAs even when only part of the batch is long.
+int32_t auto_partition(const pa_cache_desc* c, int32_t batch, int32_t num_q_heads, int64_t cap) {
+    const int32_t unit = partition_unit(c->block_size);
+    const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * groups;
+    const int64_t want = 8ll * sm_count();
+    const int64_t whole = (cap + unit - 1) / unit * unit;
+    if (units >= want) return static_cast<int32_t>(std::max<int64_t>(whole, unit));
+    const int32_t cands[] = {8192, 4096, 2048, 1024, 512};
+    for (int32_t p : cands) {
+        if (p % unit != 0 || p >= whole) continue;
+        if (units * ((cap + p - 1) / p) >= want) return p;
+    }
+    return std::min<int32_t>(512, static_cast<int32_t>(std::max<int64_t>(whole, unit)));
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                            int32_t max_blocks_per_seq, int32_t requested) {
+    if (check_cache_desc(cache) != PA_OK || batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+        num_q_heads % cache->num_kv_heads != 0)
+        return -1;
+    const int32_t unit = partition_unit(cache->block_size);
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * cache->block_size;
+    if (cap >= (int64_t{1} << 31)) return -1;
+    if (requested == -1) return static_cast<int32_t>((cap + unit - 1) / unit * unit);
+    if (requested > 0) return requested % unit == 0 ? requested : -1;
+    if (requested == 0) return auto_partition(cache, batch, num_q_heads, cap);
+    return -1;
+}
+
+extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                           int32_t max_blocks_per_seq, int32_t partition_size) {
+    const int32_t p = pa_decode_partition_size(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
+    if (p <= 0) return 0;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * cache->block_size;
+    const int64_t parts = (cap + p - 1) / p;
+    if (parts <= 1) return 0;
+    return static_cast<size_t>(batch) * num_q_heads * parts * (cache->head_dim + 2) * sizeof(float);
+}
+
+extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                         int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t batch, float scale,
+                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                         void* out, pa_dtype out_dtype, int32_t* device_status, void* stream_) {
+    pa_status st = check_cache_desc(cache);
+    if (st != PA_OK) return st;
+    if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID;
+    if (num_q_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID;
+    if (q_dtype != PA_F32 && q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (out_dtype != PA_F32 && out_dtype != PA_F16 && out_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID;
+    if (batch == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(device_status, 4) ||
+        !aligned(workspace, 16))
+        return PA_ERR_INVALID;
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    const int64_t n_hg = (group + kHeadsPerCta - 1) / kHeadsPerCta;
+    if (batch > 65535 || cache->num_kv_heads * n_hg > 65535) return PA_ERR_UNSUPPORTED;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * cache->block_size;
+    if (cap >= (int64_t{1} << 31)) return PA_ERR_UNSUPPORTED;
+
+    const int32_t p = pa_decode_partition_size(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
+    if (p <= 0) return PA_ERR_INVALID;
+    const int64_t parts = (cap + p - 1) / p;
+    if (parts > kMaxParts) return PA_ERR_UNSUPPORTED;
+    const size_t need = pa_decode_workspace_size(cache, batch, num_q_heads, max_blocks_per_seq, p);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return PA_ERR_INVALID;
+
+    DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = need ? a.part_o + static_cast<int64_t>(batch) * num_q_heads * parts * cache->head_dim : nullptr;
+    a.status = device_status;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = cache->num_kv_heads;
+    a.head_dim = cache->head_dim;
+    a.block_size = cache->block_size;
+    a.num_blocks = cache->num_blocks;
+    a.max_blocks = max_blocks_per_seq;
+    a.group = group;
+    a.partition_size = p;
+    a.max_parts = static_cast<int32_t>(parts);
+    a.q_dtype = q_dtype;
+    a.kv_dtype = cache->kv_dtype;
+    a.out_dtype = out_dtype;
+    a.scale = scale;
+    a.k_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->k_scale : 1.f;
+    a.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
+    if (st == PA_OK && parts > 1) st = launch_decode_reduce(a, s);
+    return st;
+}

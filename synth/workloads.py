@@ -197,6 +197,37 @@ def append_tokens_f32(w, which):
     return normal_f32(w.seed, st, n).reshape(w.append_tokens, w.n_kv_heads, w.head_dim)
 
 
+def build_prefix_tables(w, allocator):
+    """Block tables of the prefix workload, made by calling ``allocator``.
+
+    ``allocator`` is anything with ``append_slot(row, n, pos, block_size)``
+    and ``fork(row, n)`` (the library's or the oracle's).  Sequence 0 writes
+    the prefix, every other sequence shares its blocks (fork), then each
+    sequence writes its private suffix and the step's new token (position
+    ``context_lens[s]``).  Only the order of calls is fixed here; block ids
+    and slots are whatever the allocator returns.  Returns ``(tables int32
+    [batch, max_blocks], decode context lengths, slots of the new tokens)``.
+    """
+    bs = w.block_size
+    rows = [[-1] * w.max_blocks for _ in range(w.batch)]
+    nblk = [0] * w.batch
+    for pos in range(w.prefix_len):
+        _, nblk[0], _ = allocator.append_slot(rows[0], nblk[0], pos, bs)
+    for s in range(1, w.batch):
+        allocator.fork(rows[0], nblk[0])
+        rows[s][:nblk[0]] = rows[0][:nblk[0]]
+        nblk[s] = nblk[0]
+    new_slots = []
+    for s in range(w.batch):
+        for pos in range(w.prefix_len, int(w.context_lens[s]) + 1):
+            slot, nblk[s], cow = allocator.append_slot(rows[s], nblk[s], pos, bs)
+            if cow is not None:
+                raise RuntimeError("the prefix blocks are full: no copy-on-write expected")
+        new_slots.append(slot)
+    tables = np.array([[max(b, 0) for b in r] for r in rows], dtype=np.int32)
+    return tables, w.context_lens.astype(np.int64) + 1, np.array(new_slots, dtype=np.int64)
+
+
 def fp8_scale_of(values_f32):
     """The per-tensor FP8 scale the workloads use: largest |value| / 448, in float32."""
     return np.float32(np.float32(np.max(np.abs(values_f32))) / np.float32(448.0))

@@ -1,0 +1,219 @@
+"""The C-ABI library on the host (no GPU needed): every declared symbol is
+exported, and the host-side entry points match the oracle bit for bit."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import cache as ocache
+from oracle import closed_forms
+from oracle.allocator import AllocError as OAllocError
+from oracle.allocator import BlockAllocator as OAlloc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "pagedattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(built_lib):
+    names = _declared()
+    assert len(names) >= 20
+    lib = ctypes.CDLL(built_lib)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_declares_every_symbol(pa):
+    from paged_kv_cache_257_gb300 import _native
+    assert set(_declared()) == set(_native.SIGNATURES)
+
+
+def test_version_and_status_strings(pa):
+    from paged_kv_cache_257_gb300 import _native
+    assert "sm_103a" in pa.version()
+    lib = _native.lib()
+    for code, name in _native.STATUS.items():
+        assert lib.pa_status_string(code).decode() == name
+
+
+@pytest.mark.parametrize("layers,hkv,d,dtype", [(40, 40, 128, "f16"), (32, 8, 128, "bf16"), (80, 8, 128, "fp8_e4m3"),
+                                                (1, 2, 64, "f32")])
+def test_kv_bytes_per_token_matches_closed_form(pa, layers, hkv, d, dtype):
+    b = closed_forms.DTYPE_BYTES[dtype]
+    assert pa.kv_bytes_per_token(layers, hkv, d, dtype) == closed_forms.kv_bytes_per_token(layers, hkv, d, b)
+    assert pa.dtype_size(dtype) == b
+
+
+def test_slot_mapping_matches_oracle(pa):
+    rng = np.random.default_rng(0)
+    for bs in (8, 16, 32):
+        tables = rng.permutation(4000)[:40 * 20].reshape(20, 40).astype(np.int32)
+        seq = rng.integers(0, 20, 500).astype(np.int32)
+        pos = rng.integers(0, 40 * bs, 500).astype(np.int32)
+        got = pa.compute_slot_mapping(tables, seq, pos, bs)
+        assert np.array_equal(got, ocache.slot_mapping(tables, seq, pos, bs))
+
+
+def test_slot_mapping_rejects_bad_positions(pa):
+    tables = np.zeros((2, 3), dtype=np.int32)
+    for seq, pos in ((0, 48), (0, -1), (2, 0)):
+        with pytest.raises(pa.NativeError) as e:
+            pa.compute_slot_mapping(tables, [seq], [pos], 16)
+        assert e.value.status == "PA_ERR_RANGE"
+
+
+# ------------------------------------------------------------- allocator
+
+def _same(lib_alloc, model):
+    assert lib_alloc.dump() == model.dump()
+    assert lib_alloc.free_count == model.free_count
+
+
+@pytest.mark.parametrize("seed", [0, 1, 42, 0xC0FFEE])
+def test_allocator_handout_order(pa, seed):
+    a, m = pa.BlockAllocator(300, seed), OAlloc(300, seed)
+    _same(a, m)
+    assert [a.alloc() for _ in range(300)] == [m.alloc() for _ in range(300)]
+    _same(a, m)
+
+
+def _apply(obj, op, *args):
+    try:
+        return ("ok", getattr(obj, op)(*args))
+    except (OAllocError,) as e:
+        return ("err", e.status)
+    except Exception as e:  # library AllocError
+        if hasattr(e, "status"):
+            return ("err", e.status)
+        raise
+
+
+def test_allocator_random_trace_is_bit_exact(pa):
+    rng = np.random.default_rng(1)
+    a, m = pa.BlockAllocator(96, 7), OAlloc(96, 7)
+    rows_a, rows_m, nblk = [], [], []
+    for step in range(4000):
+        op = rng.integers(0, 6)
+        if op == 0 or not rows_a:                         # start a sequence
+            rows_a.append([-1] * 8)
+            rows_m.append([-1] * 8)
+            nblk.append(0)
+            continue
+        i = int(rng.integers(len(rows_a)))
+        if op in (1, 2):                                  # append a token at the end
+            pos = int(rng.integers(0, nblk[i] * 16 + 1))
+            ra = _apply(a, "append_slot", rows_a[i], nblk[i], pos, 16)
+            rm = _apply(m, "append_slot", rows_m[i], nblk[i], pos, 16)
+            assert ra == rm
+            assert rows_a[i] == rows_m[i]
+            if ra[0] == "ok":
+                nblk[i] = ra[1][1]
+        elif op == 3:                                     # fork
+            ra = _apply(a, "fork", rows_a[i], nblk[i])
+            rm = _apply(m, "fork", rows_m[i], nblk[i])
+            assert ra == rm
+            if ra[0] == "ok":
+                rows_a.append(list(rows_a[i]))
+                rows_m.append(list(rows_m[i]))
+                nblk.append(nblk[i])
+        elif op == 4:                                     # finish a sequence
+            ra = _apply(a, "free_sequence", rows_a[i], nblk[i])
+            rm = _apply(m, "free_sequence", rows_m[i], nblk[i])
+            assert ra == rm
+            rows_a.pop(i), rows_m.pop(i), nblk.pop(i)
+        else:                                             # raw single-block calls, some invalid
+            b = int(rng.integers(-2, 100))
+            fn = ("incref", "decref", "cow")[int(rng.integers(3))]
+            assert _apply(a, fn, b) == _apply(m, fn, b)
+        _same(a, m)
+
+
+def test_allocator_cow_scenario_matches_model(pa):
+    for alloc in (pa.BlockAllocator(10), OAlloc(10)):
+        row, n = [-1] * 4, 0
+        for pos in range(20):
+            _, n, _ = alloc.append_slot(row, n, pos, 16)
+        alloc.fork(row, n)
+        child = list(row)
+        slot, _, cow = alloc.append_slot(child, n, 20, 16)
+        assert cow == (1, 2) and slot == 2 * 16 + 4
+
+
+def test_allocator_errors(pa):
+    a = pa.BlockAllocator(1)
+    a.alloc()
+    with pytest.raises(pa.AllocError) as e:
+        a.alloc()
+    assert e.value.status == "OOM"
+    with pytest.raises(pa.AllocError) as e:
+        a.incref(5)
+    assert e.value.status == "RANGE"
+    with pytest.raises(pa.AllocError):
+        pa.BlockAllocator(0)
+
+
+# ------------------------------------------------- host-side validation
+
+def _call_decode(pa, desc, **over):
+    from paged_kv_cache_257_gb300 import _native
+    lib = _native.lib()
+    args = dict(q=8192, q_dtype=2, hq=32, k=8192, v=8192, bt=8192, max_blocks=256, ctx=8192, batch=4,
+                scale=0.088, part=0, ws=None, ws_bytes=0, out=8192, out_dtype=0)
+    args.update(over)
+    c = desc.c()
+    return lib.pa_decode_attention(ctypes.byref(c), args["q"], args["q_dtype"], args["hq"], args["k"], args["v"],
+                                   args["bt"], args["max_blocks"], args["ctx"], args["batch"], args["scale"],
+                                   args["part"], args["ws"], args["ws_bytes"], args["out"], args["out_dtype"],
+                                   None, None)
+
+
+def test_decode_rejects_bad_arguments_before_any_launch(pa):
+    d = pa.CacheDesc(1024, 16, 8, 128, "bf16")
+    assert _call_decode(pa, d, q=None) == 1
+    assert _call_decode(pa, d, hq=30) == 1                       # not a multiple of Hkv
+    assert _call_decode(pa, d, q=8194) == 1                      # misaligned
+    assert _call_decode(pa, d, part=24) == 1                     # not a multiple of 16
+    assert _call_decode(pa, d, ws=None, ws_bytes=0) == 1         # split needs a workspace
+    assert _call_decode(pa, d, out_dtype=3) == 4                 # FP8 output unsupported
+    assert _call_decode(pa, d, scale=float("inf")) == 1
+    assert _call_decode(pa, d, batch=0) == 0                     # empty batch: no-op
+    assert _call_decode(pa, pa.CacheDesc(1024, 16, 8, 96, "bf16")) == 4
+    assert _call_decode(pa, pa.CacheDesc(1024, 12, 8, 128, "bf16")) == 4
+    assert _call_decode(pa, pa.CacheDesc(1024, 16, 8, 128, "fp8_e4m3", 0.0, 1.0)) == 1
+
+
+def test_append_rejects_bad_arguments(pa):
+    from paged_kv_cache_257_gb300 import _native
+    lib = _native.lib()
+    c = pa.CacheDesc(64, 16, 2, 64, "bf16").c()
+    ok = dict(k=4096, v=4096, src=2, slots=4096, n=3, kc=4096, vc=4096)
+
+    def call(**o):
+        a = dict(ok)
+        a.update(o)
+        return lib.pa_kv_append(ctypes.byref(c), a["k"], a["v"], a["src"], a["slots"], a["n"], a["kc"], a["vc"],
+                                None, None)
+    assert call(n=0) == 0
+    assert call(k=None) == 1
+    assert call(src=1) == 4               # f16 source into a bf16 cache
+    assert call(slots=4100) == 1          # int64 slots misaligned
+    assert call(n=-1) == 1
+
+
+def test_workspace_and_partition_sizes(pa):
+    d = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
+    assert pa.partition_size(d, 4, 64, 8192, 512) == 512
+    assert pa.decode_workspace_size(d, 4, 64, 8192, 512) == 4 * 64 * 256 * 130 * 4
+    assert pa.partition_size(d, 4, 64, 8192, -1) == 131072
+    assert pa.decode_workspace_size(d, 4, 64, 8192, -1) == 0
+    assert pa.partition_size(d, 4, 64, 8192, 100) == -1
+    auto = pa.partition_size(d, 4, 64, 8192, 0)
+    assert auto > 0 and auto % 16 == 0
