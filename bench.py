@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--partition", type=int, default=None, help="tokens per partition (default: the workload's)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle baseline sample")
+    p.add_argument("--clock-probe-s", type=float, default=2.0,
+                   help="seconds of untimed load before the timed steps, for the clock sampler")
     return p.parse_args()
 
 
@@ -192,7 +194,7 @@ class GpuWorkload:
         self.workspace = None
         need = pa.decode_workspace_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], self.partition)
         if need:
-            self.workspace = torch.empty(need, dtype=torch.uint8, device=device)
+            self.workspace = pa.new_workspace(need, device)
         self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
         self.resolved_partition = pa.partition_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1],
                                                     self.partition)
@@ -240,11 +242,21 @@ class GpuWorkload:
         return n + 1 + (1 if self.workspace is not None else 0)
 
 
-def time_device(wk, steps, warmup):
-    """Timed region: barrier + synchronize, K steps, synchronize; per-decode events too."""
+def time_device(wk, steps, warmup, probe_s=0.0):
+    """Timed region: barrier + synchronize, K steps, synchronize; per-decode events too.
+
+    ``probe_s`` seconds of extra untimed steps run first so that the clock
+    sampler (nvidia-smi, 200 ms period) sees the GPU under this load."""
     torch = wk.torch
     for i in range(warmup):
         wk.step(i)
+    torch.cuda.synchronize()
+    t0, i = time.perf_counter(), warmup
+    while time.perf_counter() - t0 < probe_s:
+        wk.step(i)
+        i += 1
+        if i % 256 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -408,7 +420,7 @@ def main():
     replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
     wk = GpuWorkload(args.workload, device, replicas, args.partition)
     with ClockSampler(local) as clk:
-        total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup)
+        total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
     e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
     total_ms = max_over_ranks(total_ms)
     e2e_ms = max_over_ranks(e2e_ms)
@@ -436,7 +448,7 @@ def main():
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window=f"{args.clock_probe_s:.1f} s of the same steps + the timed steps"),
     }
     if wk.unique_kv_bytes != wk.kv_bytes:
         line["unique_kv_gbs"] = wk.unique_kv_bytes * world / step_s / 1e9

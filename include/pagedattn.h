@@ -163,8 +163,11 @@ int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int3
                                  int32_t max_blocks_per_seq, int32_t requested);
 
 /* Bytes of device workspace pa_decode_attention needs for these arguments
- * (partial softmax state of the split-context partitions; 0 when one
- * partition covers every sequence).  Returns 0 also for invalid input. */
+ * (merge counters and the partial softmax state of the split-context
+ * partitions; 0 when one partition covers every sequence).  Returns 0 also
+ * for invalid input.  The workspace must be zero-filled before its first
+ * use; every completed call leaves its counters at zero again, so one
+ * zeroed buffer serves any sequence of calls that are not concurrent. */
 size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                 int32_t max_blocks_per_seq, int32_t partition_size);
 
@@ -177,7 +180,8 @@ size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32
  * "The PagedAttention CUDA Kernel" (read the query, look up the block table,
  * fetch K and V from scattered blocks).  Long contexts are split into
  * partitions of `partition_size` tokens whose partial results are merged by
- * log-sum-exp in a second kernel.
+ * log-sum-exp: by the last partition's CTA when a sequence has at most 16
+ * partitions, otherwise by a second kernel.
  *   q              device [batch][num_q_heads][head_dim] of q_dtype
  *   block_tables   device [batch][max_blocks_per_seq] int32
  *   context_lens   device [batch] int32, cached tokens per sequence (0 gives
@@ -185,7 +189,9 @@ size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32
  *   scale          softmax scale (1/sqrt(head_dim) for the usual attention)
  *   partition_size as in pa_decode_partition_size
  *   workspace      device buffer of at least pa_decode_workspace_size()
- *                  bytes (may be NULL when that size is 0); 16-byte aligned
+ *                  bytes (may be NULL when that size is 0); 16-byte aligned,
+ *                  zero-filled before its first use; calls sharing one
+ *                  workspace must not run concurrently
  *   out            device [batch][num_q_heads][head_dim] of out_dtype
  *                  (PA_F32, PA_F16 or PA_BF16)
  * Supported: head_dim 64/128/256; num_q_heads a multiple of num_kv_heads;

@@ -155,7 +155,7 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
     od = _dtype_of(out, "out")
     need = decode_workspace_size(desc, batch, hq, max_blocks, partition)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = new_workspace(need, q.device)
     c = desc.c()
     st = lib().pa_decode_attention(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
                                    _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
@@ -163,6 +163,11 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
                                    need if need else 0, _ptr(out), DTYPE[od], _ptr(status), _stream(stream))
     check("pa_decode_attention", st)
     return out
+
+
+def new_workspace(nbytes, device="cuda"):
+    """A zero-filled decode workspace (the library keeps its counters zero between calls)."""
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
 
 
 def new_status(device="cuda"):
@@ -273,4 +278,4 @@ class BlockAllocator:
 
 __all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
            "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size",
-           "decode_workspace_size", "decode_attention", "new_status", "read_device_status"]
+           "decode_workspace_size", "decode_attention", "new_status", "new_workspace", "read_device_status"]

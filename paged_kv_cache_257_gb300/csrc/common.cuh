@@ -53,6 +53,33 @@ __device__ __forceinline__ void store_out(void* p, int64_t i, float x, pa_dtype 
     else static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
 }
 
+// ------------------------------------------- programmatic dependent launch
+//
+// Kernels are launched with programmatic stream serialisation: a kernel may
+// be scheduled while its predecessor in the stream is still running, so every
+// kernel waits (pdl_wait) before touching global memory, and lets its
+// successor be scheduled early (pdl_trigger).  Both are no-ops for a kernel
+// launched without the attribute.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ----------------------------------------------------------- fast math
 
 // 2^x by the hardware ex2 instruction (ex2(-inf) = +0).
@@ -181,13 +208,13 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
     return y;
 }
 
-// Two E4M3 codes (low byte -> low half) to two exact float16 values.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes_in_low16) {
-    uint32_t y;
-    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-        : "=r"(y)
-        : "r"(two_codes_in_low16));
-    return y;
+// Four E4M3 codes (bytes 0..3 of x) to two exact float16 pairs: bytes 0, 1 go
+// to `lo` (low half first), bytes 2, 3 to `hi`.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 __device__ __forceinline__ uint32_t byte_perm(uint32_t x, uint32_t y, uint32_t sel) {

@@ -19,6 +19,8 @@ struct DecodeArgs {
     void* out;                    // [batch][num_q_heads][head_dim] of out_dtype
     float* part_o;                // [batch][num_q_heads][max_parts][head_dim] (split only)
     float* part_ml;               // [batch][num_q_heads][max_parts][2]: (max, sum) in log2 units
+    int32_t* tickets;             // [batch][num_kv_heads * head groups], zero between calls
+    int32_t fused_merge;          // 1: the last CTA of a group merges; 0: the merge kernel does
     int32_t* status;              // device status word or null
     int32_t batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks;
     int32_t group;                // num_q_heads / num_kv_heads
@@ -31,6 +33,9 @@ struct DecodeArgs {
 
 // Query heads one CTA serves (a KV head's group is split into chunks of this).
 constexpr int kHeadsPerCta = 8;
+
+// Up to this many partitions per sequence the decode kernel merges them itself.
+constexpr int kFusedMergeMaxParts = 16;
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

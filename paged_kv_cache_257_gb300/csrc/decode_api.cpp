@@ -12,6 +12,23 @@ namespace {
 
 constexpr int kMaxParts = 32768;
 
+// Workspace layout of a split call: merge tickets, then partial outputs, then
+// partial (max, sum) pairs.
+struct WorkspaceLayout {
+    size_t tickets_bytes, part_o_bytes, part_ml_bytes;
+    size_t total() const { return tickets_bytes + part_o_bytes + part_ml_bytes; }
+};
+
+WorkspaceLayout layout(const pa_cache_desc* c, int64_t batch, int64_t num_q_heads, int64_t parts) {
+    const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
+    WorkspaceLayout w{};
+    if (parts <= 1) return w;
+    w.tickets_bytes = (static_cast<size_t>(batch * c->num_kv_heads * groups) * sizeof(int32_t) + 255) / 256 * 256;
+    w.part_o_bytes = static_cast<size_t>(batch * num_q_heads * parts * c->head_dim) * sizeof(float);
+    w.part_ml_bytes = static_cast<size_t>(batch * num_q_heads * parts * 2) * sizeof(float);
+    return w;
+}
+
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
 
 // Tokens per partition must be a multiple of the 16-token chunk and of the block size.
@@ -23,15 +40,15 @@ int32_t auto_partition(const pa_cache_desc* c, int32_t batch, int32_t num_q_head
     const int32_t unit = partition_unit(c->block_size);
     const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
     const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * groups;
-    const int64_t want = 8ll * sm_count();
+    const int64_t want = 16ll * sm_count();
     const int64_t whole = (cap + unit - 1) / unit * unit;
     if (units >= want) return static_cast<int32_t>(std::max<int64_t>(whole, unit));
-    const int32_t cands[] = {8192, 4096, 2048, 1024, 512};
+    const int32_t cands[] = {8192, 4096, 2048, 1024, 512, 256};
     for (int32_t p : cands) {
         if (p % unit != 0 || p >= whole) continue;
         if (units * ((cap + p - 1) / p) >= want) return p;
     }
-    return std::min<int32_t>(512, static_cast<int32_t>(std::max<int64_t>(whole, unit)));
+    return std::min<int32_t>(256, static_cast<int32_t>(std::max<int64_t>(whole, unit)));
 }
 
 }  // namespace
@@ -58,9 +75,7 @@ extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t b
     const int32_t p = pa_decode_partition_size(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
     if (p <= 0) return 0;
     const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * cache->block_size;
-    const int64_t parts = (cap + p - 1) / p;
-    if (parts <= 1) return 0;
-    return static_cast<size_t>(batch) * num_q_heads * parts * (cache->head_dim + 2) * sizeof(float);
+    return layout(cache, batch, num_q_heads, (cap + p - 1) / p).total();
 }
 
 extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
@@ -102,8 +117,12 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.out = out;
-    a.part_o = static_cast<float*>(workspace);
-    a.part_ml = need ? a.part_o + static_cast<int64_t>(batch) * num_q_heads * parts * cache->head_dim : nullptr;
+    const WorkspaceLayout wl = layout(cache, batch, num_q_heads, parts);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.tickets = need ? reinterpret_cast<int32_t*>(ws) : nullptr;
+    a.part_o = need ? reinterpret_cast<float*>(ws + wl.tickets_bytes) : nullptr;
+    a.part_ml = need ? reinterpret_cast<float*>(ws + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
+    a.fused_merge = parts <= kFusedMergeMaxParts ? 1 : 0;
     a.status = device_status;
     a.batch = batch;
     a.num_q_heads = num_q_heads;
@@ -124,6 +143,6 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
     st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
-    if (st == PA_OK && parts > 1) st = launch_decode_reduce(a, s);
+    if (st == PA_OK && parts > 1 && !a.fused_merge) st = launch_decode_reduce(a, s);
     return st;
 }

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "decode.h"
+#include "decode_epilogue.cuh"
 
 namespace pa {
 namespace {
@@ -53,12 +54,69 @@ struct Cfg {
     static constexpr int kMergeFloats = kConsumers * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
     static constexpr int kDataBytes = kRingBytes > kMergeFloats * 4 ? kRingBytes : kMergeFloats * 4;
     static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NSTAGES * 8 + 16;
-    static_assert(NSTAGES % kConsumers == 0, "stage s must always belong to warp s % 4");
     static_assert(kD * kElemBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
+    // Chunk c goes to stage c % NSTAGES and to consumer warp c % 4.  With
+    // NSTAGES a multiple of 4 every stage always belongs to the same warp, so
+    // that warp waits on the stage's phases strictly one after another and a
+    // parity wait can never match a phase two fills old.  Any other depth
+    // breaks that and must not be built.
+    static_assert(NSTAGES % kConsumers == 0, "each stage must belong to exactly one consumer warp");
 };
 
+// Ring depth (16-token chunks in flight per CTA): a multiple of the consumer
+// warp count, small enough that 4 CTAs fit an SM.
+#ifndef PA_DECODE_STAGES_16BIT
+#define PA_DECODE_STAGES_16BIT 4
+#endif
+#ifndef PA_DECODE_STAGES_FP8
+#define PA_DECODE_STAGES_FP8 8
+#endif
+
+// Largest growth (log2 units) of a chunk's score maximum over the running
+// reference before the accumulators are rescaled.
+constexpr float kLazyRescale = 8.f;
+
+// O^T[128 d][8 heads] += V^T P^T for one 16-token chunk held in stage `vb`.
+// 16-bit caches: ldmatrix.trans gives the A fragments directly.  FP8: each
+// ldmatrix.trans register holds (token 2q: d, d+1 | token 2q+1: d, d+1); a
+// byte permute regroups it into token pairs at a fixed d before widening, so
+// m-tile rows interleave d (row i <-> d = 16 mt + 2 i, row i + 8 <-> + 1).
+template <pa_dtype KV, typename C, bool MASK>
+__device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t v_row, int v_sel, int sw,
+                                         uint32_t pb0, uint32_t pb1, uint32_t vm01, uint32_t vm23) {
+    if constexpr (KV != PA_FP8_E4M3) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t ar[4];
+            ldsm_x4_t(vb + (mt >> 2) * C::kRegionBytes + v_row + ((((mt & 3) * 2 + v_sel) ^ sw) << 4), ar[0], ar[1],
+                      ar[2], ar[3]);
+            if constexpr (MASK) {
+                ar[0] &= vm01; ar[1] &= vm01; ar[2] &= vm23; ar[3] &= vm23;
+            }
+            mma_16816<KV == PA_BF16>(o[mt], ar, pb0, pb1);
+        }
+    } else {
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vb + v_row + (((2 * c2 + v_sel) ^ sw) << 4), r0, r1, r2, r3);
+            uint32_t ar[4], br[4];
+            e4m3x4_to_f16x2x2(byte_perm(r0, 0, 0x3120), ar[0], ar[1]);   // tokens 0..7, d / d+1
+            e4m3x4_to_f16x2x2(byte_perm(r2, 0, 0x3120), ar[2], ar[3]);   // tokens 8..15
+            e4m3x4_to_f16x2x2(byte_perm(r1, 0, 0x3120), br[0], br[1]);
+            e4m3x4_to_f16x2x2(byte_perm(r3, 0, 0x3120), br[2], br[3]);
+            if constexpr (MASK) {
+                ar[0] &= vm01; ar[1] &= vm01; ar[2] &= vm23; ar[3] &= vm23;
+                br[0] &= vm01; br[1] &= vm01; br[2] &= vm23; br[3] &= vm23;
+            }
+            mma_16816<false>(o[2 * c2], ar, pb0, pb1);
+            mma_16816<false>(o[2 * c2 + 1], br, pb0, pb1);
+        }
+    }
+}
+
 template <pa_dtype KV, int BS, int NSTAGES>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeArgs a) {
     using C = Cfg<KV, BS, NSTAGES>;
@@ -78,6 +136,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int kvh = blockIdx.y / n_hg, hg = blockIdx.y - kvh * n_hg;
     const int part = blockIdx.x;
 
+    pdl_wait();      // inputs may come from the previous kernel in the stream
+    pdl_trigger();
     int ctx = __ldg(a.context_lens + seq);
     const int cap = a.max_blocks * BS;
     if (ctx < 0 || ctx > cap) {
@@ -205,18 +265,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     // FP8 tiles arrive as 4 consecutive codes per k pair (see the K loop):
                     // k rows (2q, 2q+1) <-> d = 16kk + 4q + {0,1}, (2q+8, 2q+9) <-> d + {2,3}
                     const int64_t e = qrow + 16 * kk + 4 * q4;
-                    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                    if (hv) {
-                        if (a.q_dtype == PA_BF16) {
-                            x0 = to_float<PA_BF16>(a.q, e); x1 = to_float<PA_BF16>(a.q, e + 1);
-                            x2 = to_float<PA_BF16>(a.q, e + 2); x3 = to_float<PA_BF16>(a.q, e + 3);
-                        } else {
-                            x0 = to_float<PA_F16>(a.q, e); x1 = to_float<PA_F16>(a.q, e + 1);
-                            x2 = to_float<PA_F16>(a.q, e + 2); x3 = to_float<PA_F16>(a.q, e + 3);
-                        }
+                    const uint2 raw = hv ? __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.q) + e))
+                                         : make_uint2(0u, 0u);
+                    if (a.q_dtype == PA_BF16) {   // bf16 -> float (exact) -> f16
+                        qf[kk][0] = pack2<false>(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
+                        qf[kk][1] = pack2<false>(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+                    } else {
+                        qf[kk][0] = raw.x;
+                        qf[kk][1] = raw.y;
                     }
-                    qf[kk][0] = pack2<false>(x0, x1);
-                    qf[kk][1] = pack2<false>(x2, x3);
                 }
             }
         }
@@ -241,8 +298,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const uint32_t kb = ring + st * C::kStageBytes;
             const uint32_t vb = kb + C::kTileBytes;
 
-            // ---- S^T[16 tokens][8 heads] = K Q^T
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S^T[16 tokens][8 heads] = K Q^T, as two independent accumulation chains
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (!kFp8) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -250,25 +307,27 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                     const uint32_t addr = kb + (kk >> 2) * C::kRegionBytes + k_row +
                                           ((((kk & 3) * 2 + k_sel) ^ sw) << 4);
                     ldsm_x4(addr, ar[0], ar[1], ar[2], ar[3]);
-                    mma_16816<kBf16>(s, ar, qf[kk][0], qf[kk][1]);
+                    mma_16816<kBf16>((kk & 1) ? sb : sa, ar, qf[kk][0], qf[kk][1]);
                 }
             } else {
 #pragma unroll
                 for (int c2 = 0; c2 < 4; ++c2) {
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(kb + k_row + (((2 * c2 + k_sel) ^ sw) << 4), r0, r1, r2, r3);
-                    uint32_t ar[4] = {e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
-                                      e4m3x2_to_f16x2(r1 >> 16)};
-                    mma_16816<false>(s, ar, qf[2 * c2][0], qf[2 * c2][1]);
-                    uint32_t br[4] = {e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
-                                      e4m3x2_to_f16x2(r3 >> 16)};
-                    mma_16816<false>(s, br, qf[2 * c2 + 1][0], qf[2 * c2 + 1][1]);
+                    uint32_t ar[4], br[4];
+                    e4m3x4_to_f16x2x2(r0, ar[0], ar[2]);   // row g:   d+{0,1} | d+{2,3}
+                    e4m3x4_to_f16x2x2(r1, ar[1], ar[3]);   // row g+8
+                    mma_16816<false>(sa, ar, qf[2 * c2][0], qf[2 * c2][1]);
+                    e4m3x4_to_f16x2x2(r2, br[0], br[2]);
+                    e4m3x4_to_f16x2x2(r3, br[1], br[3]);
+                    mma_16816<false>(sb, br, qf[2 * c2 + 1][0], qf[2 * c2 + 1][1]);
                 }
             }
 
             // ---- online softmax over this chunk (log2 domain)
             const int valid = tok1 - (tok0 + c * kChunk);   // >= 1; < 16 only in the last chunk
-            float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
+            float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
+            float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
             if (valid < kChunk) {
                 if (g >= valid) x0 = x1 = kNegInf;
                 if (g + 8 >= valid) x2 = x3 = kNegInf;
@@ -279,57 +338,38 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, off));
                 cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, off));
             }
-            const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
-            const float mu0 = mn0 == kNegInf ? 0.f : mn0, mu1 = mn1 == kNegInf ? 0.f : mn1;
-            const float al0 = exp2_approx(m0 - mu0), al1 = exp2_approx(m1 - mu1);
-            const float p0 = exp2_approx(x0 - mu0), p2 = exp2_approx(x2 - mu0);
-            const float p1 = exp2_approx(x1 - mu1), p3 = exp2_approx(x3 - mu1);
-            l0 = l0 * al0 + p0 + p2;
-            l1 = l1 * al1 + p1 + p3;
-            m0 = mn0;
-            m1 = mn1;
+            // The reference maximum moves only when a score exceeds it by more than
+            // 2^kLazyRescale; until then p <= 2^kLazyRescale and (m, l, o) stay
+            // consistent, so the rescale of o is skipped on most chunks.
+            if (__any_sync(0xffffffffu, cm0 > m0 + kLazyRescale || cm1 > m1 + kLazyRescale)) {
+                const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
+                const float al0 = exp2_approx(m0 - mn0), al1 = exp2_approx(m1 - mn1);   // 0 on the first chunk
+                l0 *= al0;
+                l1 *= al1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                o[i][0] *= al0; o[i][1] *= al1;
-                o[i][2] *= al0; o[i][3] *= al1;
+                for (int i = 0; i < 8; ++i) {
+                    o[i][0] *= al0; o[i][1] *= al1;
+                    o[i][2] *= al0; o[i][3] *= al1;
+                }
+                m0 = mn0;
+                m1 = mn1;
             }
+            const float p0 = exp2_approx(x0 - m0), p2 = exp2_approx(x2 - m0);
+            const float p1 = exp2_approx(x1 - m1), p3 = exp2_approx(x3 - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
             // P^T as the B operand: (token, head) pairs transposed to (head, token)
             const uint32_t pb0 = movmatrix_t(pack2<kBf16>(p0, p1));   // tokens 0..7
             const uint32_t pb1 = movmatrix_t(pack2<kBf16>(p2, p3));   // tokens 8..15
 
-            // tokens past the context keep stale data in the stage: zero their V
-            uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+            // ---- O^T[128 d][8 heads] += V^T P^T; in the last chunk the rows past
+            // the context hold stale stage data, so their V is zeroed first
             if (valid < kChunk) {
-                vm01 = (2 * q4 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-                vm23 = (2 * q4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < valid ? 0xffff0000u : 0u);
-            }
-
-            // ---- O^T[128 d][8 heads] += V^T P^T
-            if constexpr (!kFp8) {
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    uint32_t ar[4];
-                    const uint32_t addr = vb + (mt >> 2) * C::kRegionBytes + v_row +
-                                          ((((mt & 3) * 2 + v_sel) ^ sw) << 4);
-                    ldsm_x4_t(addr, ar[0], ar[1], ar[2], ar[3]);
-                    ar[0] &= vm01; ar[1] &= vm01; ar[2] &= vm23; ar[3] &= vm23;
-                    mma_16816<kBf16>(o[mt], ar, pb0, pb1);
-                }
+                const uint32_t vm01 = (2 * q4 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
+                const uint32_t vm23 = (2 * q4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < valid ? 0xffff0000u : 0u);
+                pv_chunk<KV, C, true>(o, vb, v_row, v_sel, sw, pb0, pb1, vm01, vm23);
             } else {
-#pragma unroll
-                for (int c2 = 0; c2 < 4; ++c2) {
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vb + v_row + (((2 * c2 + v_sel) ^ sw) << 4), r0, r1, r2, r3);
-                    // r = [tok 2q: d, d+1 | tok 2q+1: d, d+1] -> pairs over tokens at fixed d
-                    const uint32_t x0p = byte_perm(r0, 0, 0x3120), y0p = byte_perm(r2, 0, 0x3120);
-                    const uint32_t x1p = byte_perm(r1, 0, 0x3120), y1p = byte_perm(r3, 0, 0x3120);
-                    uint32_t ar[4] = {e4m3x2_to_f16x2(x0p) & vm01, e4m3x2_to_f16x2(x0p >> 16) & vm01,
-                                      e4m3x2_to_f16x2(y0p) & vm23, e4m3x2_to_f16x2(y0p >> 16) & vm23};
-                    mma_16816<false>(o[2 * c2], ar, pb0, pb1);
-                    uint32_t br[4] = {e4m3x2_to_f16x2(x1p) & vm01, e4m3x2_to_f16x2(x1p >> 16) & vm01,
-                                      e4m3x2_to_f16x2(y1p) & vm23, e4m3x2_to_f16x2(y1p >> 16) & vm23};
-                    mma_16816<false>(o[2 * c2 + 1], br, pb0, pb1);
-                }
+                pv_chunk<KV, C, false>(o, vb, v_row, v_sel, sw, pb0, pb1, 0u, 0u);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(empty + st));
@@ -398,6 +438,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             }
         }
     }
+    if (n_parts > 1 && a.fused_merge) merge_if_last(a, seq, h0, nh, n_parts);
 }
 
 // ------------------------------------------------------------ host side
@@ -454,8 +495,8 @@ pa_status launch(const DecodeArgs& a, cudaStream_t stream) {
         return PA_ERR_CUDA;
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
     dim3 grid(a.max_parts, a.num_kv_heads * n_hg, a.batch);
-    kernel<<<grid, kThreads, C::kSmemBytes, stream>>>(mk, mv, a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (launch_pdl(kernel, grid, dim3(kThreads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
 }
 
 template <pa_dtype KV, int NSTAGES>
@@ -480,9 +521,9 @@ bool mma_path_supported(const DecodeArgs& a) {
 
 pa_status launch_decode_mma(const DecodeArgs& a, cudaStream_t stream) {
     switch (a.kv_dtype) {
-        case PA_BF16: return launch_bs<PA_BF16, 8>(a, stream);
-        case PA_F16: return launch_bs<PA_F16, 8>(a, stream);
-        case PA_FP8_E4M3: return launch_bs<PA_FP8_E4M3, 8>(a, stream);
+        case PA_BF16: return launch_bs<PA_BF16, PA_DECODE_STAGES_16BIT>(a, stream);
+        case PA_F16: return launch_bs<PA_F16, PA_DECODE_STAGES_16BIT>(a, stream);
+        case PA_FP8_E4M3: return launch_bs<PA_FP8_E4M3, PA_DECODE_STAGES_FP8>(a, stream);
         default: return PA_ERR_UNSUPPORTED;
     }
 }

@@ -16,7 +16,9 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kUnroll = 8;   // independent partial loads in flight per lane
 constexpr float kNegInf = -__builtin_huge_valf();
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* scratch) {
@@ -29,15 +31,22 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* scrat
     if (lane == 0) scratch[warp] = v;
     __syncthreads();
     float r = scratch[0];
-    for (int w = 1; w < kThreads / 32; ++w) r = is_max ? fmaxf(r, scratch[w]) : r + scratch[w];
+    for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, scratch[w]) : r + scratch[w];
     __syncthreads();
     return r;
 }
 
+// One CTA per (query head, sequence, 32-wide slice of head_dim).  Warp w sums
+// partitions w, w+8, ... for the 32 output elements (one per lane, coalesced
+// 128-byte rows), kUnroll loads at a time; the 8 warp sums meet in shared memory.
 __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArgs a) {
     extern __shared__ float weights[];
-    __shared__ float scratch[kThreads / 32];
+    __shared__ float scratch[kWarps];
+    __shared__ float sums[kWarps][32];
     const int hq = blockIdx.x, seq = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();      // inputs may come from the previous kernel in the stream
+    pdl_trigger();
     int ctx = __ldg(a.context_lens + seq);
     const int cap = a.max_blocks * a.block_size;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
@@ -45,7 +54,8 @@ __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArg
     if (n_parts <= 1) return;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + hq;
     const float* ml = a.part_ml + row * a.max_parts * 2;
-    const float* po = a.part_o + row * a.max_parts * a.head_dim;
+    const int d = blockIdx.z * 32 + lane;
+    const float* po = a.part_o + row * a.max_parts * a.head_dim + d;
 
     float M = kNegInf;
     for (int p = threadIdx.x; p < n_parts; p += kThreads) M = fmaxf(M, ml[2 * p]);
@@ -58,11 +68,29 @@ __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArg
         L += w;
     }
     L = block_reduce(L, false, scratch);  // its barriers also publish `weights`
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int d = threadIdx.x; d < a.head_dim; d += kThreads) {
-        float acc = 0.f;
-        for (int p = 0; p < n_parts; ++p) acc = fmaf(weights[p], po[static_cast<int64_t>(p) * a.head_dim + d], acc);
-        store_out(a.out, row * a.head_dim + d, acc * inv, a.out_dtype);
+
+    float acc[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) acc[u] = 0.f;
+    int p = warp;
+    for (; p + (kUnroll - 1) * kWarps < n_parts; p += kUnroll * kWarps) {
+        float v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = po[static_cast<int64_t>(p + u * kWarps) * a.head_dim];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) acc[u] = fmaf(weights[p + u * kWarps], v[u], acc[u]);
+    }
+    for (; p < n_parts; p += kWarps) acc[0] = fmaf(weights[p], po[static_cast<int64_t>(p) * a.head_dim], acc[0]);
+    float sum = 0.f;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) sum += acc[u];
+    sums[warp][lane] = sum;
+    __syncthreads();
+    if (warp == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += sums[w][lane];
+        store_out(a.out, row * a.head_dim + d, L > 0.f ? t / L : 0.f, a.out_dtype);
     }
 }
 
@@ -75,9 +103,9 @@ pa_status launch_decode_reduce(const DecodeArgs& a, cudaStream_t stream) {
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
         if (err != cudaSuccess) return PA_ERR_CUDA;
     }
-    dim3 grid(a.num_q_heads, a.batch);
-    decode_reduce_kernel<<<grid, kThreads, smem, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    dim3 grid(a.num_q_heads, a.batch, a.head_dim / 32);
+    if (launch_pdl(decode_reduce_kernel, grid, dim3(kThreads), smem, stream, a) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
 }
 
 }  // namespace pa

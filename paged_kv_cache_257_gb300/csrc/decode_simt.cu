@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "decode.h"
+#include "decode_epilogue.cuh"
 
 namespace pa {
 namespace {
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
     const int part = blockIdx.x;
     const int bs = a.block_size;
 
+    pdl_wait();      // inputs may come from the previous kernel in the stream
+    pdl_trigger();
     int ctx = __ldg(a.context_lens + seq);
     const int cap = a.max_blocks * bs;
     if (ctx < 0 || ctx > cap) {
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
             }
         }
     }
+    if (n_parts > 1 && a.fused_merge) merge_if_last(a, seq, h0, nh, n_parts);
 }
 
 template <pa_dtype KV, int D>
@@ -165,7 +169,7 @@ pa_status launch(const DecodeArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return PA_ERR_CUDA;
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
     dim3 grid(a.max_parts, a.num_kv_heads * n_hg, a.batch);
-    kernel<<<grid, kWarps * 32, smem, stream>>>(a);
+    if (launch_pdl(kernel, grid, dim3(kWarps * 32), smem, stream, a) != cudaSuccess) return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

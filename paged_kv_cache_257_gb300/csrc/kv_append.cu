@@ -83,6 +83,8 @@ kv_append_kernel(const void* __restrict__ k, const void* __restrict__ v, const i
                  int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                  int64_t num_slots, void* __restrict__ k_cache, void* __restrict__ v_cache, float k_scale,
                  float v_scale, int32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t packs_per_row = head_dim / kPack;
     const int64_t per_tensor = static_cast<int64_t>(num_tokens) * num_kv_heads * packs_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ src,
                    const int32_t* __restrict__ dst, int32_t num_blocks, int64_t block_vec16,
                    int32_t* __restrict__ status) {
+    pdl_wait();
+    pdl_trigger();
     const int32_t pair = blockIdx.y;
     const int32_t s = __ldg(src + pair), d = __ldg(dst + pair);
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
@@ -156,16 +160,16 @@ using namespace pa;
 namespace {
 
 template <pa_dtype SRC, pa_dtype DST>
-void launch_append(const pa_cache_desc* c, const void* k, const void* v, const int64_t* slots, int32_t n,
+cudaError_t launch_append(const pa_cache_desc* c, const void* k, const void* v, const int64_t* slots, int32_t n,
                    void* kc, void* vc, int32_t* status, cudaStream_t stream) {
     const int64_t total = 2ll * n * c->num_kv_heads * (c->head_dim / kPack);
     const int64_t want = (total + kAppendThreads - 1) / kAppendThreads;
     const int blocks = static_cast<int>(std::min<int64_t>(want, 16ll * sm_count()));
     const float ks = DST == PA_FP8_E4M3 ? c->k_scale : 1.f;
     const float vs = DST == PA_FP8_E4M3 ? c->v_scale : 1.f;
-    kv_append_kernel<SRC, DST><<<blocks, kAppendThreads, 0, stream>>>(
-        k, v, slots, n, c->num_kv_heads, c->head_dim, c->block_size,
-        static_cast<int64_t>(c->num_blocks) * c->block_size, kc, vc, ks, vs, status);
+    return launch_pdl(kv_append_kernel<SRC, DST>, dim3(blocks), dim3(kAppendThreads), 0, stream, k, v, slots, n,
+                      c->num_kv_heads, c->head_dim, c->block_size,
+                      static_cast<int64_t>(c->num_blocks) * c->block_size, kc, vc, ks, vs, status);
 }
 
 }  // namespace
@@ -183,7 +187,8 @@ extern "C" pa_status pa_kv_append(const pa_cache_desc* cache, const void* k, con
         return PA_ERR_INVALID;
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
     const pa_dtype dst = cache->kv_dtype;
-#define PA_APPEND(SRC_, DST_) launch_append<SRC_, DST_>(cache, k, v, slot_mapping, num_tokens, k_cache, v_cache, device_status, s)
+    cudaError_t e;
+#define PA_APPEND(SRC_, DST_) e = launch_append<SRC_, DST_>(cache, k, v, slot_mapping, num_tokens, k_cache, v_cache, device_status, s)
     if (dst == PA_F32 && src_dtype == PA_F32) PA_APPEND(PA_F32, PA_F32);
     else if (dst == PA_F16 && src_dtype == PA_F16) PA_APPEND(PA_F16, PA_F16);
     else if (dst == PA_BF16 && src_dtype == PA_BF16) PA_APPEND(PA_BF16, PA_BF16);
@@ -194,7 +199,7 @@ extern "C" pa_status pa_kv_append(const pa_cache_desc* cache, const void* k, con
     else if (dst == PA_FP8_E4M3 && src_dtype == PA_BF16) PA_APPEND(PA_BF16, PA_FP8_E4M3);
     else return PA_ERR_UNSUPPORTED;
 #undef PA_APPEND
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status pa_copy_blocks(const pa_cache_desc* cache, void* k_cache, void* v_cache,
@@ -211,10 +216,10 @@ extern "C" pa_status pa_copy_blocks(const pa_cache_desc* cache, void* k_cache, v
     const int64_t vec = block_bytes / 16;
     const int gx = static_cast<int>(std::min<int64_t>((vec + kAppendThreads - 1) / kAppendThreads, 64));
     dim3 grid(gx, num_pairs, 2);
-    copy_blocks_kernel<<<grid, kAppendThreads, 0, static_cast<cudaStream_t>(stream_)>>>(
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_blocks, dst_blocks, cache->num_blocks,
-        vec, device_status);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(kAppendThreads), 0, static_cast<cudaStream_t>(stream_),
+                               static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_blocks, dst_blocks,
+                               cache->num_blocks, vec, device_status);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status pa_read_device_status(int32_t* device_status, int32_t* flags_out, int32_t reset,

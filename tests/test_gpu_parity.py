@@ -155,3 +155,23 @@ def test_fp8_append_is_bit_exact_on_edge_values(pa, cuda):
         got = kc[1, 0, 1].cpu().numpy()
         from oracle import e4m3
         assert np.array_equal(got, e4m3.quantize(src[0, 0], scale))
+
+
+@pytest.mark.parametrize("partition", [64, 512])   # 47 partitions: merge kernel; 6: fused merge
+def test_workspace_counters_return_to_zero_and_reuse(pa, cuda, partition):
+    case = Case(batch=3, hq=8, hkv=2, d=128, bs=16, kv_dtype="bf16", q_dtype="bf16", ctx=[3000, 700, 1], seed=9)
+    kc, vc = case.gpu_pools(pa, cuda)
+    kp, vp = case.oracle_pools()
+    expect = case.oracle_out(kp, vp)
+    desc = case.desc(pa)
+    need = pa.decode_workspace_size(desc, 3, 8, case.max_blocks, partition)
+    ws = pa.new_workspace(need, cuda)
+    q = to_torch(case.q_store, "bf16", cuda)
+    bt = torch.from_numpy(case.tables).to(cuda)
+    cl = torch.from_numpy(case.ctx).to(cuda)
+    for _ in range(3):   # the same workspace, call after call
+        out = pa.decode_attention(desc, q, kc, vc, bt, cl, case.scale, partition=partition, workspace=ws)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), expect, TOL["bf16"], f"reuse P={partition}")
+        tickets = ws[:256].view(torch.int32)
+        assert int(tickets.abs().sum()) == 0
