@@ -206,6 +206,36 @@ pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtyp
                               int32_t partition_size, void* workspace, size_t workspace_bytes,
                               void* out, pa_dtype out_dtype, int32_t* device_status, void* stream);
 
+/* pa_decode_attention for callers that cannot allocate device memory (the
+ * pages have no counterpart: this serves the library's users).  Some callers
+ * cannot call cudaMalloc: code inside a host framework or server that owns
+ * all device memory through its own allocator and forbids other allocations,
+ * decode loops that must not stall every stream on cudaMalloc's implicit
+ * device synchronisation, and deployments whose device footprint is fixed
+ * up front.  This entry point takes the same arguments as
+ * pa_decode_attention except the workspace: the split-context workspace is a
+ * static array of PA_NOALLOC_SCRATCH_BYTES in device memory that every GPU
+ * loading the library holds until the process exits.  It allocates nothing
+ * and calls no allocating routine; the caller still passes every input and
+ * output.
+ *   - PA_ERR_RANGE when pa_decode_workspace_size() for these arguments
+ *     exceeds PA_NOALLOC_SCRATCH_BYTES (use larger partitions, a smaller
+ *     batch, or pa_decode_attention with a caller-owned workspace).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and zero-fills it, synchronising the device; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call clears the merge counters it needs on its
+ *     stream before the kernels.  Calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race on the array: serialise them. */
+#define PA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                      int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t batch, float scale,
+                                      int32_t partition_size, void* out, pa_dtype out_dtype,
+                                      int32_t* device_status, void* stream);
+
 /* Wait for `stream`, copy the device status word to *flags_out (may be
  * NULL) and, if `reset` is non-zero, zero it.  Returns PA_ERR_DEVICE_FLAG
  * if any flag was set, PA_OK otherwise. */

@@ -23,6 +23,7 @@ DEVFLAG_SLOT_RANGE = 1
 DEVFLAG_BLOCK_RANGE = 2
 DEVFLAG_CONTEXT_RANGE = 4
 DEVFLAG_TIMEOUT = 8
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES
 
 
 class CacheDescC(ctypes.Structure):
@@ -49,6 +50,9 @@ SIGNATURES = {
     "pa_decode_attention": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p, c_void_p,
                                            c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p, c_size_t,
                                            c_void_p, ctypes.c_int, c_void_p, c_void_p]),
+    "pa_decode_attention_noalloc": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p,
+                                                   c_void_p, c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p,
+                                                   ctypes.c_int, c_void_p, c_void_p]),
     "pa_read_device_status": (ctypes.c_int, [c_void_p, P_int32, c_int32, c_void_p]),
     "pa_alloc_create": (ctypes.c_int, [c_int32, c_uint64, ctypes.POINTER(c_void_p)]),
     "pa_alloc_destroy": (None, [c_void_p]),

@@ -165,6 +165,30 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
+def decode_attention_noalloc(desc, q, k_cache, v_cache, block_tables, context_lens, scale, partition=0, out=None,
+                             out_dtype=None, status=None, stream=None):
+    """``pa_decode_attention_noalloc``: decode attention with the library's static workspace.
+
+    For callers that must not allocate device memory (the library's own array
+    of 8 MiB per GPU replaces the workspace); ``out`` must then be passed in.
+    Raises NativeError("PA_ERR_RANGE") when the problem's workspace does not fit.
+    """
+    _need(q, "q")
+    _need(block_tables, "block_tables", torch.int32)
+    _need(context_lens, "context_lens", torch.int32)
+    batch, hq, d = q.shape
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=TORCH_STORAGE[out_dtype or "f32"], device=q.device)
+    _need(out, "out")
+    c = desc.c()
+    st = lib().pa_decode_attention_noalloc(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
+                                           _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                           _ptr(context_lens), batch, float(scale), partition, _ptr(out),
+                                           DTYPE[_dtype_of(out, "out")], _ptr(status), _stream(stream))
+    check("pa_decode_attention_noalloc", st)
+    return out
+
+
 def new_workspace(nbytes, device="cuda"):
     """A zero-filled decode workspace (the library keeps its counters zero between calls)."""
     return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
@@ -278,4 +302,4 @@ class BlockAllocator:
 
 __all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
            "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size",
-           "decode_workspace_size", "decode_attention", "new_status", "new_workspace", "read_device_status"]
+           "decode_workspace_size", "decode_attention", "decode_attention_noalloc", "new_status", "new_workspace", "read_device_status"]

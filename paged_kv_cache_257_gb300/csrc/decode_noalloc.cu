@@ -1,0 +1,71 @@
+// Decode attention that allocates nothing, for callers that cannot call
+// cudaMalloc: code running inside a host framework or server that owns all
+// device memory through its own allocator and forbids other allocations,
+// decode loops that must not stall every stream on the implicit device
+// synchronisation of cudaMalloc, and deployments whose device memory
+// footprint is fixed up front.  The caller still passes every input and
+// output buffer; only the split-context workspace comes from a fixed array
+// in device memory that this library owns.
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "decode.h"
+#include "pagedattn.h"
+
+namespace {
+
+// The workspace of pa_decode_attention_noalloc.  Every GPU that loads the
+// library holds one copy of this array until the process exits.
+static_assert(PA_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte alignment");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_mutex;
+std::vector<void*> g_scratch_ptr;   // device address of the array, per device (null: not set up)
+
+// Device address of the array on the current device.  In host code the
+// array's name stands for a host-side shadow, never the device memory, so
+// the address is asked of the runtime once per device (with that device
+// current) and cached; the array is also zero-filled then.
+pa_status scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (dev >= static_cast<int>(g_scratch_ptr.size())) g_scratch_ptr.resize(dev + 1, nullptr);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
+        if (cudaMemset(p, 0, PA_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                 const int32_t* context_lens, int32_t batch, float scale,
+                                                 int32_t partition_size, void* out, pa_dtype out_dtype,
+                                                 int32_t* device_status, void* stream) {
+    const size_t need = pa_decode_workspace_size(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
+    if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_RANGE;
+    void* ws = nullptr;
+    if (need > 0 && q && k_cache && v_cache && block_tables && context_lens && out) {
+        pa_status st = scratch_address(&ws);
+        if (st != PA_OK) return st;
+        // The array keeps the previous call's contents.  Its front holds one
+        // merge counter per (sequence, KV head, head group), which must start
+        // at zero: clear them on the caller's stream, ahead of the kernels.
+        const int64_t groups = (num_q_heads / cache->num_kv_heads + pa::kHeadsPerCta - 1) / pa::kHeadsPerCta;
+        const size_t counters = static_cast<size_t>(batch) * cache->num_kv_heads * groups * sizeof(int32_t);
+        if (cudaMemsetAsync(ws, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return pa_decode_attention(cache, q, q_dtype, num_q_heads, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                               context_lens, batch, scale, partition_size, ws, need, out, out_dtype, device_status,
+                               stream);
+}

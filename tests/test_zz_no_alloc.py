@@ -1,0 +1,68 @@
+"""The allocation-free decode entry point, for callers that cannot allocate
+device memory (a host framework that owns every device allocation, a decode
+loop that must not stall on cudaMalloc's device synchronisation, a fixed
+footprint).  It must give the same output as the ordinary entry point, call
+after call, while its workspace is the library's own static array.
+
+This file is collected last on purpose: a run that stops at the first
+failure has then already run every other test."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from harness import TOL, Case, assert_close, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(pa, cuda, case):
+    kc, vc = case.gpu_pools(pa, cuda)
+    q = to_torch(case.q_store, case.q_dtype, cuda)
+    bt = torch.from_numpy(case.tables).to(cuda)
+    cl = torch.from_numpy(case.ctx).to(cuda)
+    return kc, vc, q, bt, cl
+
+
+def _noalloc_call(pa, case, q, kc, vc, bt, cl, partition, out):
+    """One call straight through the C ABI (no binding-side allocation)."""
+    from paged_kv_cache_257_gb300 import _native
+    c = case.desc(pa).c()
+    return _native.lib().pa_decode_attention_noalloc(
+        ctypes.byref(c), q.data_ptr(), _native.DTYPE[case.q_dtype], case.hq, kc.data_ptr(), vc.data_ptr(),
+        bt.data_ptr(), bt.shape[1], cl.data_ptr(), case.batch, case.scale, partition, out.data_ptr(),
+        _native.DTYPE["f32"], None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
+@pytest.mark.parametrize("kv,q,partition", [("bf16", "bf16", 256),      # few partitions: fused merge
+                                             ("bf16", "bf16", 32),       # many partitions: merge kernel
+                                             ("fp8_e4m3", "bf16", 512),
+                                             ("f32", "f32", 64)])        # CUDA-core kernel
+def test_noalloc_matches_the_ordinary_entry_point_twice(pa, cuda, kv, q, partition):
+    case = Case(batch=4, hq=16, hkv=4, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[3000, 700, 1, 129], seed=21)
+    kc, vc, qt, bt, cl = _inputs(pa, cuda, case)
+    expect = pa.decode_attention(case.desc(pa), qt, kc, vc, bt, cl, case.scale, partition=partition)
+    expect = expect.cpu().numpy()
+    for call in range(2):   # the static workspace keeps the first call's contents for the second
+        out = torch.full((case.batch, case.hq, case.d), float("nan"), dtype=torch.float32, device=cuda)
+        st = _noalloc_call(pa, case, qt, kc, vc, bt, cl, partition, out)
+        assert st == 0, f"call {call}: status {st}"
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), expect, TOL[kv], f"no-alloc call {call}")
+
+
+def test_noalloc_rejects_workspaces_beyond_its_array(pa, cuda):
+    # 4 x 64 heads x 256 partitions of 512 tokens need ~34 MB of partials: more than the 8 MiB array
+    from paged_kv_cache_257_gb300 import _native
+    desc = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
+    assert pa.decode_workspace_size(desc, 4, 64, 8192, 512) > _native.NOALLOC_SCRATCH_BYTES
+    q = torch.zeros((4, 64, 128), dtype=torch.bfloat16, device=cuda)
+    bt = torch.zeros((4, 8192), dtype=torch.int32, device=cuda)
+    cl = torch.zeros(4, dtype=torch.int32, device=cuda)
+    out = torch.zeros((4, 64, 128), dtype=torch.float32, device=cuda)
+    with pytest.raises(pa.NativeError) as e:
+        pa.decode_attention_noalloc(desc, q, q, q, bt, cl, 0.088, partition=512, out=out)
+    assert e.value.status == "PA_ERR_RANGE"
+    assert np.all(out.cpu().numpy() == 0)          # nothing was launched
