@@ -162,9 +162,9 @@ pa_status pa_copy_blocks(const pa_cache_desc* cache, void* k_cache, void* v_cach
 int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                  int32_t max_blocks_per_seq, int32_t requested);
 
-/* Bytes of device workspace pa_decode_attention needs for these arguments
- * (merge counters and the partial softmax state of the split-context
- * partitions; 0 when one partition covers every sequence).  Returns 0 also
+/* Bytes of device workspace pa_decode_attention needs for these arguments:
+ * 256 bytes of work-scheduling counters, plus, when contexts are split, the
+ * merge counters and the partial softmax state of the partitions.  Returns 0
  * for invalid input.  The workspace must be zero-filled before its first
  * use; every completed call leaves its counters at zero again, so one
  * zeroed buffer serves any sequence of calls that are not concurrent. */
@@ -189,7 +189,7 @@ size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32
  *   scale          softmax scale (1/sqrt(head_dim) for the usual attention)
  *   partition_size as in pa_decode_partition_size
  *   workspace      device buffer of at least pa_decode_workspace_size()
- *                  bytes (may be NULL when that size is 0); 16-byte aligned,
+ *                  bytes; 16-byte aligned,
  *                  zero-filled before its first use; calls sharing one
  *                  workspace must not run concurrently
  *   out            device [batch][num_q_heads][head_dim] of out_dtype

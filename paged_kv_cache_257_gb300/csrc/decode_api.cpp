@@ -12,16 +12,25 @@ namespace {
 
 constexpr int kMaxParts = 32768;
 
-// Workspace layout of a split call: merge tickets, then partial outputs, then
-// partial (max, sum) pairs.
+// 1: batches up to kMaxPersistentBatch run the persistent tensor-core kernel;
+// 0: every batch runs one CTA per work item.
+#ifndef PA_DECODE_PERSISTENT
+#define PA_DECODE_PERSISTENT 0
+#endif
+
+// Workspace layout: scheduler counters (256 B), then for a split call the
+// merge tickets, partial outputs and partial (max, sum) pairs.
+constexpr size_t kSchedBytes = 256;
+
 struct WorkspaceLayout {
-    size_t tickets_bytes, part_o_bytes, part_ml_bytes;
-    size_t total() const { return tickets_bytes + part_o_bytes + part_ml_bytes; }
+    size_t sched_bytes, tickets_bytes, part_o_bytes, part_ml_bytes;
+    size_t total() const { return sched_bytes + tickets_bytes + part_o_bytes + part_ml_bytes; }
 };
 
 WorkspaceLayout layout(const pa_cache_desc* c, int64_t batch, int64_t num_q_heads, int64_t parts) {
     const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
     WorkspaceLayout w{};
+    w.sched_bytes = kSchedBytes;
     if (parts <= 1) return w;
     w.tickets_bytes = (static_cast<size_t>(batch * c->num_kv_heads * groups) * sizeof(int32_t) + 255) / 256 * 256;
     w.part_o_bytes = static_cast<size_t>(batch * num_q_heads * parts * c->head_dim) * sizeof(float);
@@ -69,6 +78,19 @@ extern "C" int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t 
     if (requested == 0) return auto_partition(cache, batch, num_q_heads, cap);
     return -1;
 }
+
+namespace pa {
+
+size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                            int32_t partition_size) {
+    const int32_t p = pa_decode_partition_size(c, batch, num_q_heads, max_blocks, partition_size);
+    if (p <= 0) return 0;
+    const int64_t cap = static_cast<int64_t>(max_blocks) * c->block_size;
+    const WorkspaceLayout w = layout(c, batch, num_q_heads, (cap + p - 1) / p);
+    return w.sched_bytes + w.tickets_bytes;
+}
+
+}  // namespace pa
 
 extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                            int32_t max_blocks_per_seq, int32_t partition_size) {
@@ -119,9 +141,11 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     a.out = out;
     const WorkspaceLayout wl = layout(cache, batch, num_q_heads, parts);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    a.tickets = need ? reinterpret_cast<int32_t*>(ws) : nullptr;
-    a.part_o = need ? reinterpret_cast<float*>(ws + wl.tickets_bytes) : nullptr;
-    a.part_ml = need ? reinterpret_cast<float*>(ws + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
+    a.sched = reinterpret_cast<int32_t*>(ws);
+    const bool split = wl.tickets_bytes > 0;
+    a.tickets = split ? reinterpret_cast<int32_t*>(ws + wl.sched_bytes) : nullptr;
+    a.part_o = split ? reinterpret_cast<float*>(ws + wl.sched_bytes + wl.tickets_bytes) : nullptr;
+    a.part_ml = split ? reinterpret_cast<float*>(ws + wl.sched_bytes + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
     a.fused_merge = parts <= kFusedMergeMaxParts ? 1 : 0;
     a.status = device_status;
     a.batch = batch;
@@ -142,6 +166,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     a.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
+    a.persistent = (PA_DECODE_PERSISTENT && batch <= kMaxPersistentBatch) ? 1 : 0;
     st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
     if (st == PA_OK && parts > 1 && !a.fused_merge) st = launch_decode_reduce(a, s);
     return st;

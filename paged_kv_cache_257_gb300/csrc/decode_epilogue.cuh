@@ -16,33 +16,36 @@
 
 namespace pa {
 
-__device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int seq, int h0, int nh, int n_parts) {
+// Run by `nthreads` threads (ids `tid`) that synchronise through `bar`;
+// `grp` indexes the (sequence, KV head, head group) ticket.
+template <typename Bar>
+__device__ __forceinline__ void merge_group_if_last(const DecodeArgs& a, int seq, int grp, int h0, int nh,
+                                                    int n_parts, int tid, int nthreads, Bar bar) {
     __shared__ int s_last;
     __shared__ float s_m[kHeadsPerCta][kFusedMergeMaxParts];
     __shared__ float s_w[kHeadsPerCta][kFusedMergeMaxParts];
-    const int grp = seq * gridDim.y + blockIdx.y;   // (sequence, KV head, head group)
-    __syncthreads();                                // every partial of this CTA is written
-    if (threadIdx.x == 0) {
+    bar();                                          // every partial of this CTA is written
+    if (tid == 0) {
         __threadfence();                            // ... and visible before the ticket
         const bool last = atomicAdd(a.tickets + grp, 1) == n_parts - 1;
         if (last) __threadfence();                  // the other CTAs' partials are visible
         s_last = last;
     }
-    __syncthreads();
+    bar();
     if (!s_last) return;
     const float neg_inf = -__builtin_huge_valf();
     const int D = a.head_dim;
     const int64_t row0 = static_cast<int64_t>(seq) * a.num_q_heads + h0;
     // every (head, partition) pair's max and sum, one per thread
-    for (int i = threadIdx.x; i < nh * n_parts; i += blockDim.x) {
+    for (int i = tid; i < nh * n_parts; i += nthreads) {
         const int h = i / n_parts, p = i - h * n_parts;
         const float* ml = a.part_ml + ((row0 + h) * a.max_parts + p) * 2;
         s_m[h][p] = __ldcg(ml);
         s_w[h][p] = __ldcg(ml + 1);
     }
-    __syncthreads();
-    if (threadIdx.x < nh) {                         // per head: weights normalised by their sum
-        const int h = threadIdx.x;
+    bar();
+    if (tid < nh) {                                 // per head: weights normalised by their sum
+        const int h = tid;
         float M = neg_inf;
         for (int p = 0; p < n_parts; ++p) M = fmaxf(M, s_m[h][p]);
         float L = 0.f;
@@ -54,8 +57,8 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int seq, int 
         const float inv = L > 0.f ? 1.f / L : 0.f;
         for (int p = 0; p < n_parts; ++p) s_w[h][p] *= inv;
     }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < nh * D; idx += blockDim.x) {
+    bar();
+    for (int idx = tid; idx < nh * D; idx += nthreads) {
         const int h = idx / D, d = idx - h * D;
         const float* po = a.part_o + (row0 + h) * a.max_parts * D + d;
         float v[kFusedMergeMaxParts];
@@ -66,7 +69,7 @@ __device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int seq, int 
         for (int p = 0; p < kFusedMergeMaxParts; ++p) acc = p < n_parts ? fmaf(s_w[h][p], v[p], acc) : acc;
         store_out(a.out, (row0 + h) * D + d, acc, a.out_dtype);
     }
-    if (threadIdx.x == 0) a.tickets[grp] = 0;
+    if (tid == 0) a.tickets[grp] = 0;
 }
 
 }  // namespace pa

@@ -7,23 +7,26 @@
 // gives softmax(Q K^T / sqrt(d_k)) V; section 2 Example 2: several query
 // heads share one KV head (query head h reads KV head h / G).
 //
-// One CTA serves one (partition of the context, KV head, sequence) and up to
-// eight query heads of that KV head's group.  Four consumer warps and one
-// producer warp:
-//   * the producer walks the block table (32 ids per coalesced load) and
-//     streams each 16-token chunk's K and V tiles into a ring of shared
+// A work item is one (sequence, KV head, group of up to 8 of its query heads,
+// partition of the context).  A CTA has four consumer warps and one producer
+// warp:
+//   * the producer walks the item's block table (32 ids per coalesced load)
+//     and streams each 16-token chunk's K and V tiles into a ring of shared
 //     memory stages with 2-D TMA loads (128-byte swizzle, evict-first L2
-//     hint), signalling an mbarrier per stage;
-//   * consumer warp w takes chunks w, w+4, ...; for each it forms
-//     S^T = K Q^T with mma.sync m16n8k16 (16 tokens x 8 heads, the heads on
-//     the N side so G = 8 needs no padding), runs the online softmax in
-//     registers, turns P into the B operand with two movmatrix transposes
-//     and accumulates O^T = V^T P^T (8 tiles of 16 rows of head_dim);
-//   * the warps' (max, sum, output) states are merged in shared memory and
-//     written either as the final output or, for a split context, as a
-//     partition partial that a second kernel merges.
-// FP8 tiles are widened to float16 in registers (exact), with the K scale
-// folded into the score scale and the V scale into the output.
+//     hint), arming an mbarrier per stage;
+//   * the consumer warp owning a chunk forms S^T = K Q^T with mma.sync
+//     m16n8k16 (16 tokens x 8 heads, heads on the N side so G = 8 needs no
+//     padding), runs the online softmax in registers, turns P into the B
+//     operand with two movmatrix transposes and accumulates O^T = V^T P^T;
+//   * the warps' (max, sum, output) states are merged and written as the
+//     final output or, for a split context, as a partition partial.
+// Two kernels share these pieces.  The persistent kernel (batches up to
+// kMaxPersistentBatch) runs one CTA per resident slot; each CTA takes items
+// from an atomic counter -- every full partition first, partial ones after --
+// and its producer streams the next item's tiles while the consumers finish
+// and merge the current one.  The grid kernel runs one CTA per item.
+// FP8 tiles are widened to float16 in registers, with the K scale folded into
+// the score scale and the V scale into the output.
 #include <algorithm>
 #include <mutex>
 
@@ -38,8 +41,15 @@ constexpr int kD = 128;
 constexpr int kChunk = 16;        // tokens per mma row tile
 constexpr int kConsumers = 4;     // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
-constexpr int kMergeStride = kD + 4;  // floats per head row in the merge buffer (bank spread)
+constexpr int kMergeStride = kD + 4;  // floats per head row in merge buffers (bank spread)
 constexpr float kNegInf = -__builtin_huge_valf();
+
+// 1: 16-bit tiles with 16-row boxes move as one 3-D TMA box (128-byte
+// column halves as the outermost box dimension, so shared memory still holds
+// [half][row][128 B]); 0: one 2-D box per half.
+#ifndef PA_TMA_3D
+#define PA_TMA_3D 1
+#endif
 
 template <pa_dtype KV, int BS, int NSTAGES>
 struct Cfg {
@@ -51,11 +61,9 @@ struct Cfg {
     static constexpr int kBoxRows = BS < kChunk ? BS : kChunk;
     static constexpr int kBoxBytes = kBoxRows * 128;
     static constexpr int kRingBytes = NSTAGES * kStageBytes;
-    static constexpr int kMergeFloats = kConsumers * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
-    static constexpr int kDataBytes = kRingBytes > kMergeFloats * 4 ? kRingBytes : kMergeFloats * 4;
-    static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NSTAGES * 8 + 16;
+    static constexpr bool k3D = PA_TMA_3D && kHalves == 2 && kBoxRows == kChunk;   // one box per tile
     static_assert(kD * kElemBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
-    // Chunk c goes to stage c % NSTAGES and to consumer warp c % 4.  With
+    // Chunk k goes to stage k % NSTAGES and to consumer warp k % 4.  With
     // NSTAGES a multiple of 4 every stage always belongs to the same warp, so
     // that warp waits on the stage's phases strictly one after another and a
     // parity wait can never match a phase two fills old.  Any other depth
@@ -72,15 +80,67 @@ struct Cfg {
 #define PA_DECODE_STAGES_FP8 8
 #endif
 
+// How FP8 tiles are widened to float16 for the tensor cores.
+//  0: cvt.rn.f16x2.e4m3x2 on pairs of codes (exact values).  The default: on
+//     the long-context FP8 workload it ran 242 us against 273 us for 1.
+//  1: move bit fields.  A float16 holding an E4M3 code's sign, exponent and
+//     mantissa bits in place (exponent bias 15 instead of 7) equals the E4M3
+//     value times 2^-8, subnormals included, so the scales absorb 2^8.  Four
+//     codes take 7 integer operations and no byte permute.
+#ifndef PA_FP8_WIDEN_BITS
+#define PA_FP8_WIDEN_BITS 0
+#endif
+constexpr float kFp8WidenScale = PA_FP8_WIDEN_BITS ? 256.f : 1.f;
+
+#if PA_FP8_WIDEN_BITS
+// codes 0, 2 -> `even` (low, high half), codes 1, 3 -> `odd`; values x 2^-8
+__device__ __forceinline__ void e4m3_fields_to_f16(uint32_t x, uint32_t& even, uint32_t& odd) {
+    odd = (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
+    even = ((x << 8) & 0x80008000u) | ((x << 7) & 0x3F803F80u);
+}
+#endif
+
+// K operand: the four codes a thread holds of one row (d+0..3) as the A
+// fragment's (k 2q, 2q+1) and (k 2q+8, 2q+9) registers.  Which d lands in
+// which k is matched by the query permutation in fp8_q_pairs.
+__device__ __forceinline__ void fp8_k_pairs(uint32_t x, uint32_t& k01, uint32_t& k89) {
+#if PA_FP8_WIDEN_BITS
+    e4m3_fields_to_f16(x, k01, k89);          // d+{0,2} | d+{1,3}
+#else
+    e4m3x4_to_f16x2x2(x, k01, k89);           // d+{0,1} | d+{2,3}
+#endif
+}
+
+// The query's float16 values at d+0..3 (h0..h3) in the same k order.
+__device__ __forceinline__ void fp8_q_pairs(uint32_t h01, uint32_t h23, uint32_t& k01, uint32_t& k89) {
+#if PA_FP8_WIDEN_BITS
+    k01 = __byte_perm(h01, h23, 0x5410);      // h0, h2
+    k89 = __byte_perm(h01, h23, 0x7632);      // h1, h3
+#else
+    k01 = h01;
+    k89 = h23;
+#endif
+}
+
+// V operand: an ldmatrix.trans register (token 2q: d, d+1 | token 2q+1: d, d+1)
+// as the token pairs at d and at d+1.
+__device__ __forceinline__ void fp8_v_pairs(uint32_t x, uint32_t& at_d, uint32_t& at_d1) {
+#if PA_FP8_WIDEN_BITS
+    e4m3_fields_to_f16(x, at_d, at_d1);
+#else
+    e4m3x4_to_f16x2x2(__byte_perm(x, 0, 0x3120), at_d, at_d1);
+#endif
+}
+
 // Largest growth (log2 units) of a chunk's score maximum over the running
 // reference before the accumulators are rescaled.
 constexpr float kLazyRescale = 8.f;
 
 // O^T[128 d][8 heads] += V^T P^T for one 16-token chunk held in stage `vb`.
 // 16-bit caches: ldmatrix.trans gives the A fragments directly.  FP8: each
-// ldmatrix.trans register holds (token 2q: d, d+1 | token 2q+1: d, d+1); a
-// byte permute regroups it into token pairs at a fixed d before widening, so
-// m-tile rows interleave d (row i <-> d = 16 mt + 2 i, row i + 8 <-> + 1).
+// ldmatrix.trans register holds (token 2q: d, d+1 | token 2q+1: d, d+1),
+// regrouped into token pairs at a fixed d while widening, so m-tile rows
+// interleave d (row i <-> d = 16 mt + 2 i, row i + 8 <-> + 1).
 template <pa_dtype KV, typename C, bool MASK>
 __device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t v_row, int v_sel, int sw,
                                          uint32_t pb0, uint32_t pb1, uint32_t vm01, uint32_t vm23) {
@@ -101,10 +161,10 @@ __device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t
             uint32_t r0, r1, r2, r3;
             ldsm_x4_t(vb + v_row + (((2 * c2 + v_sel) ^ sw) << 4), r0, r1, r2, r3);
             uint32_t ar[4], br[4];
-            e4m3x4_to_f16x2x2(byte_perm(r0, 0, 0x3120), ar[0], ar[1]);   // tokens 0..7, d / d+1
-            e4m3x4_to_f16x2x2(byte_perm(r2, 0, 0x3120), ar[2], ar[3]);   // tokens 8..15
-            e4m3x4_to_f16x2x2(byte_perm(r1, 0, 0x3120), br[0], br[1]);
-            e4m3x4_to_f16x2x2(byte_perm(r3, 0, 0x3120), br[2], br[3]);
+            fp8_v_pairs(r0, ar[0], ar[1]);   // tokens 0..7 at d | d+1
+            fp8_v_pairs(r2, ar[2], ar[3]);   // tokens 8..15
+            fp8_v_pairs(r1, br[0], br[1]);
+            fp8_v_pairs(r3, br[2], br[3]);
             if constexpr (MASK) {
                 ar[0] &= vm01; ar[1] &= vm01; ar[2] &= vm23; ar[3] &= vm23;
                 br[0] &= vm01; br[1] &= vm01; br[2] &= vm23; br[3] &= vm23;
@@ -115,13 +175,290 @@ __device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t
     }
 }
 
+// One consumer warp's online-softmax state for up to 8 query heads (lane
+// holds heads 2q, 2q+1) and its per-chunk step.
+template <pa_dtype KV, typename C>
+struct Consumer {
+    static constexpr bool kFp8 = KV == PA_FP8_E4M3;
+    static constexpr bool kBf16 = KV == PA_BF16;   // mma operand type: bf16, else f16
+    float o[8][4];
+    float m0, m1, l0, l1;
+    uint32_t qf[8][2];
+    int g, q4, sw, k_sel, v_sel;
+    uint32_t k_row, v_row;
+
+    __device__ __forceinline__ void init(int lane) {
+        g = lane >> 2;     // fragment group: row (token) / column (head) index
+        q4 = lane & 3;     // thread in group
+        sw = lane & 7;     // swizzle phase (row & 7 == lane & 7 for every ldmatrix below)
+        k_row = ((lane & 7) + 8 * ((lane >> 3) & 1)) * 128;   // ldmatrix rows of K
+        v_row = ((lane & 7) + 8 * (lane >> 4)) * 128;         // ldmatrix rows of V
+        k_sel = lane >> 4;                                    // K: second 16-byte column of the pair
+        v_sel = (lane >> 3) & 1;                              // V: second 16-byte column of the pair
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        m0 = m1 = kNegInf;
+        l0 = l1 = 0.f;
+    }
+
+    // Q as the B operand of S^T = K Q^T: column n = head g, 16 rows of d per
+    // k-step.  `rows` points at the first head's row (nh rows of kD 16-bit
+    // elements); GLOBAL selects read-only global loads over generic ones.
+    template <bool GLOBAL>
+    __device__ __forceinline__ void load_q(const uint16_t* rows, int nh, bool q_bf16) {
+        const bool hv = g < nh;
+        const uint16_t* row = rows + (hv ? g : 0) * kD;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if constexpr (!kFp8) {
+                const uint32_t* p0 = reinterpret_cast<const uint32_t*>(row + 16 * kk + 2 * q4);
+                const uint32_t* p1 = reinterpret_cast<const uint32_t*>(row + 16 * kk + 8 + 2 * q4);
+                qf[kk][0] = hv ? (GLOBAL ? __ldg(p0) : *p0) : 0u;
+                qf[kk][1] = hv ? (GLOBAL ? __ldg(p1) : *p1) : 0u;
+            } else {
+                // FP8 tiles give each thread 4 consecutive codes per row and k-step
+                // (d = 16kk + 4q + 0..3); fp8_q_pairs orders them like fp8_k_pairs
+                const uint2* p = reinterpret_cast<const uint2*>(row + 16 * kk + 4 * q4);
+                const uint2 raw = hv ? (GLOBAL ? __ldg(p) : *p) : make_uint2(0u, 0u);
+                uint32_t h01 = raw.x, h23 = raw.y;
+                if (q_bf16) {   // bf16 -> float (exact) -> f16
+                    h01 = pack2<false>(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
+                    h23 = pack2<false>(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
+                }
+                fp8_q_pairs(h01, h23, qf[kk][0], qf[kk][1]);
+            }
+        }
+    }
+
+    // One 16-token chunk in stage (kb: K tile, vb: V tile); `valid` tokens of
+    // it are in the context (1..16); `sc` = softmax scale x log2(e) (x K scale).
+    __device__ __forceinline__ void chunk(uint32_t kb, uint32_t vb, int valid, float sc) {
+        // ---- S^T[16 tokens][8 heads] = K Q^T, as two independent accumulation chains
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (!kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t ar[4];
+                const uint32_t addr = kb + (kk >> 2) * C::kRegionBytes + k_row + ((((kk & 3) * 2 + k_sel) ^ sw) << 4);
+                ldsm_x4(addr, ar[0], ar[1], ar[2], ar[3]);
+                mma_16816<kBf16>((kk & 1) ? sb : sa, ar, qf[kk][0], qf[kk][1]);
+            }
+        } else {
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kb + k_row + (((2 * c2 + k_sel) ^ sw) << 4), r0, r1, r2, r3);
+                uint32_t ar[4], br[4];
+                fp8_k_pairs(r0, ar[0], ar[2]);   // row g
+                fp8_k_pairs(r1, ar[1], ar[3]);   // row g+8
+                mma_16816<false>(sa, ar, qf[2 * c2][0], qf[2 * c2][1]);
+                fp8_k_pairs(r2, br[0], br[2]);
+                fp8_k_pairs(r3, br[1], br[3]);
+                mma_16816<false>(sb, br, qf[2 * c2 + 1][0], qf[2 * c2 + 1][1]);
+            }
+        }
+
+        // ---- online softmax over this chunk (log2 domain)
+        float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
+        float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
+        if (valid < kChunk) {
+            if (g >= valid) x0 = x1 = kNegInf;
+            if (g + 8 >= valid) x2 = x3 = kNegInf;
+        }
+        float cm0 = fmaxf(x0, x2), cm1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, off));
+            cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, off));
+        }
+        // The reference maximum moves only when a score exceeds it by more than
+        // 2^kLazyRescale; until then p <= 2^kLazyRescale and (m, l, o) stay
+        // consistent, so the rescale of o is skipped on most chunks.
+        if (__any_sync(0xffffffffu, cm0 > m0 + kLazyRescale || cm1 > m1 + kLazyRescale)) {
+            const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
+            const float al0 = exp2_approx(m0 - mn0), al1 = exp2_approx(m1 - mn1);   // 0 on the first chunk
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] *= al0; o[i][1] *= al1;
+                o[i][2] *= al0; o[i][3] *= al1;
+            }
+            m0 = mn0;
+            m1 = mn1;
+        }
+        const float p0 = exp2_approx(x0 - m0), p2 = exp2_approx(x2 - m0);
+        const float p1 = exp2_approx(x1 - m1), p3 = exp2_approx(x3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // P^T as the B operand: (token, head) pairs transposed to (head, token)
+        const uint32_t pb0 = movmatrix_t(pack2<kBf16>(p0, p1));   // tokens 0..7
+        const uint32_t pb1 = movmatrix_t(pack2<kBf16>(p2, p3));   // tokens 8..15
+
+        // ---- O^T[128 d][8 heads] += V^T P^T; in the last chunk the rows past
+        // the context hold stale stage data, so their V is zeroed first
+        if (valid < kChunk) {
+            const uint32_t vm01 = (2 * q4 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
+            const uint32_t vm23 = (2 * q4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < valid ? 0xffff0000u : 0u);
+            pv_chunk<KV, C, true>(o, vb, v_row, v_sel, sw, pb0, pb1, vm01, vm23);
+        } else {
+            pv_chunk<KV, C, false>(o, vb, v_row, v_sel, sw, pb0, pb1, 0u, 0u);
+        }
+    }
+
+    // Row sums were kept per lane; add over the 8 lanes sharing a head pair.
+    __device__ __forceinline__ void finish() {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+    }
+
+    // d of this lane's accumulator o[mt][0/1] (lo) and o[mt][2/3] (hi)
+    __device__ __forceinline__ int d_lo(int mt) const { return kFp8 ? 16 * mt + 2 * g : 16 * mt + g; }
+    __device__ __forceinline__ int d_hi(int mt) const { return kFp8 ? 16 * mt + 2 * g + 1 : 16 * mt + g + 8; }
+};
+
+// Producer side of one chunk: wait for its stage to be free, then arm the
+// stage's barrier and issue the TMA boxes of the K and V tiles.  `pb_a` /
+// `pb_b` are the physical blocks of the chunk's first / second block (the
+// second only for 8-token blocks).  Returns false if a wait ran out.
+template <typename C, int BS, int NSTAGES>
+__device__ __forceinline__ bool issue_chunk(const DecodeArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                            uint64_t* full, uint64_t* empty, uint32_t ring, int k, int lane, int kvh,
+                                            int t0, int tok1, int pb_a, int pb_b, uint64_t policy) {
+    const int st = k % NSTAGES;
+    if (k >= NSTAGES) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(smem_addr(empty + st), ((k / NSTAGES) - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    }
+    if (lane == 0) {
+        const bool two = BS < kChunk && t0 + BS < tok1;   // second block holds valid tokens
+        if (pb_a < 0 || pb_a >= a.num_blocks) {
+            raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
+            pb_a = a.num_blocks;   // rows past the tensor: TMA fills zeros
+        }
+        if (two && (pb_b < 0 || pb_b >= a.num_blocks)) {
+            raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
+            pb_b = a.num_blocks;
+        }
+        const int boxes = (two ? 2 : 1) * C::kHalves * 2;
+        const uint32_t fb = smem_addr(full + st);
+        mbar_arrive_expect_tx(fb, boxes * C::kBoxBytes);
+        const uint32_t kdst = ring + st * C::kStageBytes;
+        const int ya = (pb_a * a.num_kv_heads + kvh) * BS + (t0 % BS);
+        const int yb = (pb_b * a.num_kv_heads + kvh) * BS;
+        if constexpr (C::k3D) {
+            tma_load_3d(kdst, tmap_k, fb, 0, ya, 0, policy);
+            tma_load_3d(kdst + C::kTileBytes, tmap_v, fb, 0, ya, 0, policy);
+        } else {
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf) {
+                const int x = hf * (128 / C::kElemBytes);
+                const uint32_t kd = kdst + hf * C::kRegionBytes;
+                const uint32_t vd = kd + C::kTileBytes;
+                tma_load_2d(kd, tmap_k, fb, x, ya, policy);
+                tma_load_2d(vd, tmap_v, fb, x, ya, policy);
+                if (two) {
+                    tma_load_2d(kd + C::kBoxBytes, tmap_k, fb, x, yb, policy);
+                    tma_load_2d(vd + C::kBoxBytes, tmap_v, fb, x, yb, policy);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    return true;
+}
+
+// Block ids of an item's chunks, 32 at a time from one coalesced load.
+struct BlockWindow {
+    const int32_t* bt;
+    int j_first, j_end, base, my_id;
+    __device__ __forceinline__ void start(const int32_t* table, int tok0, int tok1, int bs) {
+        bt = table;
+        j_first = tok0 / bs;
+        j_end = tok1 > tok0 ? (tok1 - 1) / bs + 1 : j_first;
+        base = -32;
+        my_id = 0;
+    }
+    // the same, with the first 32 ids (blocks j_first + lane) already loaded
+    __device__ __forceinline__ void start_loaded(const int32_t* table, int tok0, int tok1, int bs, int ids) {
+        start(table, tok0, tok1, bs);
+        base = 0;
+        my_id = ids;
+    }
+    // physical blocks of the chunk starting at token t0 (second: t0 + 8, for 8-token blocks)
+    __device__ __forceinline__ void get(int t0, int bs, int lane, int& pb_a, int& pb_b) {
+        const int rel = t0 / bs - j_first;
+        if (rel >= base + 32) {
+            base = rel & ~31;
+            const int j = j_first + base + lane;
+            my_id = j < j_end ? __ldg(bt + j) : 0;
+        }
+        pb_a = __shfl_sync(0xffffffffu, my_id, rel - base);
+        pb_b = __shfl_sync(0xffffffffu, my_id, (rel + 1 - base) & 31);
+    }
+};
+
+// After the last chunk: wait until every copy this CTA issued has landed
+// (they have, unless a wait ran out) before shared memory is reused or freed.
+template <int NSTAGES>
+__device__ __forceinline__ void drain_ring(const DecodeArgs& a, uint64_t* full, int issued, int lane) {
+    if (lane != 0) return;
+    for (int st = 0; st < NSTAGES && st < issued; ++st) {
+        const int fills = (issued - st + NSTAGES - 1) / NSTAGES;
+        if (!mbar_wait(smem_addr(full + st), (fills - 1) & 1)) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
+    }
+}
+
+__device__ __forceinline__ int clamp_ctx(const DecodeArgs& a, int seq, bool report) {
+    int ctx = __ldg(a.context_lens + seq);
+    const int cap = a.max_blocks * a.block_size;
+    if (ctx < 0 || ctx > cap) {
+        if (report) raise_flag(a.status, PA_DEVFLAG_CONTEXT_RANGE);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    return ctx;
+}
+
+// Write one merged value: the final output, or this partition's partial.
+__device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, int d, int part, int n_parts,
+                                             float val, float M, float L) {
+    if (n_parts == 1) {
+        store_out(a.out, row * kD + d, val, a.out_dtype);
+    } else {
+        const int64_t pi = row * a.max_parts + part;
+        a.part_o[pi * kD + d] = val;
+        if (d == 0) {
+            a.part_ml[2 * pi] = M;
+            a.part_ml[2 * pi + 1] = L;
+        }
+    }
+}
+
+// =====================================================================
+// Grid kernel: one CTA per (partition, KV head group, sequence)
+// =====================================================================
+
+template <pa_dtype KV, int BS, int NSTAGES>
+struct GridCfg : Cfg<KV, BS, NSTAGES> {
+    using B = Cfg<KV, BS, NSTAGES>;
+    static constexpr int kMergeFloats = kConsumers * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
+    static constexpr int kDataBytes = B::kRingBytes > kMergeFloats * 4 ? B::kRingBytes : kMergeFloats * 4;
+    static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NSTAGES * 8 + 16;
+};
+
 template <pa_dtype KV, int BS, int NSTAGES>
 __global__ void __launch_bounds__(kThreads, 4)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeArgs a) {
-    using C = Cfg<KV, BS, NSTAGES>;
+    using C = GridCfg<KV, BS, NSTAGES>;
     constexpr bool kFp8 = KV == PA_FP8_E4M3;
-    constexpr bool kBf16 = KV == PA_BF16;  // mma operand type: bf16, else f16
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,12 +475,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
-    int ctx = __ldg(a.context_lens + seq);
-    const int cap = a.max_blocks * BS;
-    if (ctx < 0 || ctx > cap) {
-        if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0) raise_flag(a.status, PA_DEVFLAG_CONTEXT_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
-    }
+    const int ctx = clamp_ctx(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 1;
     if (part >= n_parts) return;
     const int tok0 = part * a.partition_size;
@@ -162,11 +494,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     __syncthreads();
 
-    // consumer state (registers), kept across the block-wide barriers below
-    float o[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+    Consumer<KV, C> cs;
+    cs.init(lane);
+    cs.reset();
 
     if (warp == kConsumers) {
         // ------------------------------------------------------ producer
@@ -175,116 +505,30 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             prefetch_tmap(&tmap_v);
         }
         const uint64_t policy = l2_evict_first_policy();
-        const int32_t* bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
-        const int j_first = tok0 / BS;
-        const int j_end = n_chunks > 0 ? (tok1 - 1) / BS + 1 : j_first;  // exclusive
-        int id_base = -32, my_id = 0;
+        BlockWindow win;
+        win.start(a.block_tables + static_cast<int64_t>(seq) * a.max_blocks, tok0, tok1, BS);
         int issued = 0;
         for (int c = 0; c < n_chunks; ++c) {
-            const int st = c % NSTAGES;
-            if (c >= NSTAGES) {
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(smem_addr(empty + st), ((c / NSTAGES) - 1) & 1);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        atomicExch(abort_flag, 1);
-                        raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-                    }
-                    break;
-                }
-                if (*reinterpret_cast<volatile int*>(abort_flag)) break;
-            }
+            if (*reinterpret_cast<volatile int*>(abort_flag)) break;
             const int t0 = tok0 + c * kChunk;
-            const int rel = t0 / BS - j_first;   // window-relative index of the chunk's first block
-            if (rel >= id_base + 32) {
-                id_base = rel & ~31;
-                const int j = j_first + id_base + lane;
-                my_id = j < j_end ? __ldg(bt + j) : 0;
-            }
-            int pb_a = __shfl_sync(0xffffffffu, my_id, rel - id_base);
-            int pb_b = 0;
-            if constexpr (BS < kChunk) pb_b = __shfl_sync(0xffffffffu, my_id, (rel + 1 - id_base) & 31);
-            if (lane == 0) {
-                const bool two = BS < kChunk && t0 + BS < tok1;   // second block holds valid tokens
-                if (pb_a < 0 || pb_a >= a.num_blocks) {
-                    raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
-                    pb_a = a.num_blocks;   // rows past the tensor: TMA fills zeros
+            int pb_a, pb_b;
+            win.get(t0, BS, lane, pb_a, pb_b);
+            if (!issue_chunk<C, BS, NSTAGES>(a, &tmap_k, &tmap_v, full, empty, ring, c, lane, kvh, t0, tok1, pb_a,
+                                             pb_b, policy)) {
+                if (lane == 0) {
+                    atomicExch(abort_flag, 1);
+                    raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
                 }
-                if (two && (pb_b < 0 || pb_b >= a.num_blocks)) {
-                    raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
-                    pb_b = a.num_blocks;
-                }
-                const int boxes = (two ? 2 : 1) * C::kHalves * 2;
-                const uint32_t fb = smem_addr(full + st);
-                mbar_arrive_expect_tx(fb, boxes * C::kBoxBytes);
-                const uint32_t kdst = ring + st * C::kStageBytes;
-                const int ya = (pb_a * a.num_kv_heads + kvh) * BS + (t0 % BS);
-                const int yb = (pb_b * a.num_kv_heads + kvh) * BS;
-#pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    const int x = hf * (128 / C::kElemBytes);
-                    const uint32_t kd = kdst + hf * C::kRegionBytes;
-                    const uint32_t vd = kd + C::kTileBytes;
-                    tma_load_2d(kd, &tmap_k, fb, x, ya, policy);
-                    tma_load_2d(vd, &tmap_v, fb, x, ya, policy);
-                    if (two) {
-                        tma_load_2d(kd + C::kBoxBytes, &tmap_k, fb, x, yb, policy);
-                        tma_load_2d(vd + C::kBoxBytes, &tmap_v, fb, x, yb, policy);
-                    }
-                }
+                break;
             }
             ++issued;
-            __syncwarp();
         }
-        // every copy this CTA issued has landed before shared memory is reused
-        if (lane == 0) {
-            for (int st = 0; st < NSTAGES && st < issued; ++st) {
-                const int fills = (issued - st + NSTAGES - 1) / NSTAGES;
-                if (!mbar_wait(smem_addr(full + st), (fills - 1) & 1)) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-            }
-        }
+        drain_ring<NSTAGES>(a, full, issued, lane);
     } else {
         // ------------------------------------------------------ consumers
-        const int g = lane >> 2;   // fragment group: row (token) / column (head) index
-        const int q4 = lane & 3;   // thread in group
-        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
-
-        // Q as the B operand of S^T = K Q^T: column n = head g, 16 rows of d per k-step
-        uint32_t qf[8][2];
-        {
-            const bool hv = g < nh;
-            const int64_t qrow = (static_cast<int64_t>(seq) * a.num_q_heads + h0 + (hv ? g : 0)) * kD;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                if constexpr (!kFp8) {
-                    const uint32_t* qp = static_cast<const uint32_t*>(a.q);
-                    qf[kk][0] = hv ? __ldg(qp + (qrow + 16 * kk + 2 * q4) / 2) : 0u;
-                    qf[kk][1] = hv ? __ldg(qp + (qrow + 16 * kk + 8 + 2 * q4) / 2) : 0u;
-                } else {
-                    // FP8 tiles arrive as 4 consecutive codes per k pair (see the K loop):
-                    // k rows (2q, 2q+1) <-> d = 16kk + 4q + {0,1}, (2q+8, 2q+9) <-> d + {2,3}
-                    const int64_t e = qrow + 16 * kk + 4 * q4;
-                    const uint2 raw = hv ? __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.q) + e))
-                                         : make_uint2(0u, 0u);
-                    if (a.q_dtype == PA_BF16) {   // bf16 -> float (exact) -> f16
-                        qf[kk][0] = pack2<false>(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
-                        qf[kk][1] = pack2<false>(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-                    } else {
-                        qf[kk][0] = raw.x;
-                        qf[kk][1] = raw.y;
-                    }
-                }
-            }
-        }
-
-        // per-lane parts of the swizzled shared-memory addresses (row & 7 == lane & 7)
-        const int sw = lane & 7;
-        const uint32_t k_row = ((lane & 7) + 8 * ((lane >> 3) & 1)) * 128;   // ldmatrix rows of K
-        const uint32_t v_row = ((lane & 7) + 8 * (lane >> 4)) * 128;         // ldmatrix rows of V
-        const int k_sel = lane >> 4;          // K: second 16-byte column of the pair
-        const int v_sel = (lane >> 3) & 1;    // V: second 16-byte column of the pair
-
+        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale * kFp8WidenScale : 1.f);
+        cs.template load_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
+                                 nh, a.q_dtype == PA_BF16);
         for (int c = warp; c < n_chunks; c += kConsumers) {
             const int st = c % NSTAGES;
             const bool landed = mbar_wait(smem_addr(full + st), (c / NSTAGES) & 1);
@@ -296,90 +540,11 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 break;
             }
             const uint32_t kb = ring + st * C::kStageBytes;
-            const uint32_t vb = kb + C::kTileBytes;
-
-            // ---- S^T[16 tokens][8 heads] = K Q^T, as two independent accumulation chains
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (!kFp8) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    uint32_t ar[4];
-                    const uint32_t addr = kb + (kk >> 2) * C::kRegionBytes + k_row +
-                                          ((((kk & 3) * 2 + k_sel) ^ sw) << 4);
-                    ldsm_x4(addr, ar[0], ar[1], ar[2], ar[3]);
-                    mma_16816<kBf16>((kk & 1) ? sb : sa, ar, qf[kk][0], qf[kk][1]);
-                }
-            } else {
-#pragma unroll
-                for (int c2 = 0; c2 < 4; ++c2) {
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kb + k_row + (((2 * c2 + k_sel) ^ sw) << 4), r0, r1, r2, r3);
-                    uint32_t ar[4], br[4];
-                    e4m3x4_to_f16x2x2(r0, ar[0], ar[2]);   // row g:   d+{0,1} | d+{2,3}
-                    e4m3x4_to_f16x2x2(r1, ar[1], ar[3]);   // row g+8
-                    mma_16816<false>(sa, ar, qf[2 * c2][0], qf[2 * c2][1]);
-                    e4m3x4_to_f16x2x2(r2, br[0], br[2]);
-                    e4m3x4_to_f16x2x2(r3, br[1], br[3]);
-                    mma_16816<false>(sb, br, qf[2 * c2 + 1][0], qf[2 * c2 + 1][1]);
-                }
-            }
-
-            // ---- online softmax over this chunk (log2 domain)
-            const int valid = tok1 - (tok0 + c * kChunk);   // >= 1; < 16 only in the last chunk
-            float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
-            float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
-            if (valid < kChunk) {
-                if (g >= valid) x0 = x1 = kNegInf;
-                if (g + 8 >= valid) x2 = x3 = kNegInf;
-            }
-            float cm0 = fmaxf(x0, x2), cm1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, off));
-                cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, off));
-            }
-            // The reference maximum moves only when a score exceeds it by more than
-            // 2^kLazyRescale; until then p <= 2^kLazyRescale and (m, l, o) stay
-            // consistent, so the rescale of o is skipped on most chunks.
-            if (__any_sync(0xffffffffu, cm0 > m0 + kLazyRescale || cm1 > m1 + kLazyRescale)) {
-                const float mn0 = fmaxf(m0, cm0), mn1 = fmaxf(m1, cm1);
-                const float al0 = exp2_approx(m0 - mn0), al1 = exp2_approx(m1 - mn1);   // 0 on the first chunk
-                l0 *= al0;
-                l1 *= al1;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    o[i][0] *= al0; o[i][1] *= al1;
-                    o[i][2] *= al0; o[i][3] *= al1;
-                }
-                m0 = mn0;
-                m1 = mn1;
-            }
-            const float p0 = exp2_approx(x0 - m0), p2 = exp2_approx(x2 - m0);
-            const float p1 = exp2_approx(x1 - m1), p3 = exp2_approx(x3 - m1);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            // P^T as the B operand: (token, head) pairs transposed to (head, token)
-            const uint32_t pb0 = movmatrix_t(pack2<kBf16>(p0, p1));   // tokens 0..7
-            const uint32_t pb1 = movmatrix_t(pack2<kBf16>(p2, p3));   // tokens 8..15
-
-            // ---- O^T[128 d][8 heads] += V^T P^T; in the last chunk the rows past
-            // the context hold stale stage data, so their V is zeroed first
-            if (valid < kChunk) {
-                const uint32_t vm01 = (2 * q4 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-                const uint32_t vm23 = (2 * q4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < valid ? 0xffff0000u : 0u);
-                pv_chunk<KV, C, true>(o, vb, v_row, v_sel, sw, pb0, pb1, vm01, vm23);
-            } else {
-                pv_chunk<KV, C, false>(o, vb, v_row, v_sel, sw, pb0, pb1, 0u, 0u);
-            }
+            cs.chunk(kb, kb + C::kTileBytes, tok1 - (tok0 + c * kChunk), sc);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(empty + st));
         }
-        // row sums were kept per lane; add over the 8 lanes sharing a head pair
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
+        cs.finish();
     }
 
     __syncthreads();  // every stage consumed (or drained): the ring becomes the merge buffer
@@ -388,30 +553,27 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     float* mm = mbuf + kConsumers * kHeadsPerCta * kMergeStride;
     float* ml = mm + kConsumers * kHeadsPerCta;
     if (warp < kConsumers) {
-        const int g = lane >> 2, q4 = lane & 3;
-        float* w0 = mbuf + (warp * kHeadsPerCta + 2 * q4) * kMergeStride;
+        float* w0 = mbuf + (warp * kHeadsPerCta + 2 * cs.q4) * kMergeStride;
         float* w1 = w0 + kMergeStride;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            const int d_lo = kFp8 ? 16 * mt + 2 * g : 16 * mt + g;
-            const int d_hi = kFp8 ? d_lo + 1 : d_lo + 8;
-            w0[d_lo] = o[mt][0];
-            w1[d_lo] = o[mt][1];
-            w0[d_hi] = o[mt][2];
-            w1[d_hi] = o[mt][3];
+            w0[cs.d_lo(mt)] = cs.o[mt][0];
+            w1[cs.d_lo(mt)] = cs.o[mt][1];
+            w0[cs.d_hi(mt)] = cs.o[mt][2];
+            w1[cs.d_hi(mt)] = cs.o[mt][3];
         }
-        if (g == 0) {
-            mm[warp * kHeadsPerCta + 2 * q4] = m0;
-            mm[warp * kHeadsPerCta + 2 * q4 + 1] = m1;
-            ml[warp * kHeadsPerCta + 2 * q4] = l0;
-            ml[warp * kHeadsPerCta + 2 * q4 + 1] = l1;
+        if (cs.g == 0) {
+            mm[warp * kHeadsPerCta + 2 * cs.q4] = cs.m0;
+            mm[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.m1;
+            ml[warp * kHeadsPerCta + 2 * cs.q4] = cs.l0;
+            ml[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.l1;
         }
     }
     __syncthreads();
 
     if (threadIdx.x < kD) {
         const int d = threadIdx.x;
-        const float vs = kFp8 ? a.v_scale : 1.f;
+        const float vs = kFp8 ? a.v_scale * kFp8WidenScale : 1.f;
         for (int h = 0; h < nh; ++h) {
             float M = kNegInf;
 #pragma unroll
@@ -424,21 +586,358 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 L += coef * ml[w * kHeadsPerCta + h];
                 acc += coef * mbuf[(w * kHeadsPerCta + h) * kMergeStride + d];
             }
-            const float val = L > 0.f ? acc * vs / L : 0.f;
             const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h0 + h;
-            if (n_parts == 1) {
-                store_out(a.out, row * kD + d, val, a.out_dtype);
-            } else {
-                const int64_t pi = row * a.max_parts + part;
-                a.part_o[pi * kD + d] = val;
-                if (d == 0) {
-                    a.part_ml[2 * pi] = M;
-                    a.part_ml[2 * pi + 1] = L;
-                }
-            }
+            store_result(a, row, d, part, n_parts, L > 0.f ? acc * vs / L : 0.f, M, L);
         }
     }
-    if (n_parts > 1 && a.fused_merge) merge_if_last(a, seq, h0, nh, n_parts);
+    if (n_parts > 1 && a.fused_merge) {
+        merge_group_if_last(a, seq, seq * gridDim.y + blockIdx.y, h0, nh, n_parts, threadIdx.x, blockDim.x,
+                            [] { __syncthreads(); });
+    }
+}
+
+// =====================================================================
+// Persistent kernel: resident CTAs take items from an atomic counter
+// =====================================================================
+
+constexpr int kQueue = 4;   // item descriptors (and their query rows) in flight per CTA
+
+// Item order: full partitions of every sequence first (sequence, partition,
+// head group), then each sequence's last, partial partition.  The producer
+// maps a counter value to an item through two prefix sums over the batch.
+struct Item {
+    int seq, grp, part, tok0, tok1, chunk0, n_chunks, n_parts;
+};
+
+template <pa_dtype KV, int BS, int NSTAGES>
+struct PersistCfg : Cfg<KV, BS, NSTAGES> {
+    using B = Cfg<KV, BS, NSTAGES>;
+    static constexpr int kQSlotBytes = kHeadsPerCta * kD * 2;                 // one item's query rows
+    static constexpr int kOffQ = B::kRingBytes;
+    static constexpr int kOffAcc = kOffQ + kQueue * kQSlotBytes;              // [8 heads][kMergeStride] f32
+    static constexpr int kOffWarpML = kOffAcc + kHeadsPerCta * kMergeStride * 4;   // [2][4 warps][8] f32
+    static constexpr int kOffPrefix = kOffWarpML + 2 * kConsumers * kHeadsPerCta * 4;  // 2 x (batch + 1) int32
+    static constexpr int kOffDesc = kOffPrefix + 2 * (kMaxPersistentBatch + 1) * 4;
+    static constexpr int kOffBars = (kOffDesc + kQueue * static_cast<int>(sizeof(Item)) + 7) / 8 * 8;
+    static constexpr int kOffFlags = kOffBars + (2 * NSTAGES + 2 * kQueue) * 8;
+    static constexpr int kSmemBytes = 1024 + kOffFlags + 16;
+};
+
+// named barrier of the four consumer warps (the producer never joins it)
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// the same barrier, returning whether `pred` held for any consumer thread:
+// every consumer warp gets the same answer, so branches on it stay uniform
+__device__ __forceinline__ bool consumer_bar_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+// largest s in [0, n) with pre[s] <= x (pre non-decreasing, pre[0] == 0)
+__device__ __forceinline__ int prefix_search(const int* pre, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <pa_dtype KV, int BS, int NSTAGES>
+__global__ void __launch_bounds__(kThreads, 4)
+decode_mma_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                             const DecodeArgs a) {
+    using C = PersistCfg<KV, BS, NSTAGES>;
+    constexpr bool kFp8 = KV == PA_FP8_E4M3;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = smem_addr(smem);
+    uint8_t* qslots = smem + C::kOffQ;
+    float* acc = reinterpret_cast<float*>(smem + C::kOffAcc);
+    float* wm = reinterpret_cast<float*>(smem + C::kOffWarpML);      // [warp][head] max
+    float* wl = wm + kConsumers * kHeadsPerCta;                       // [warp][head] sum
+    int* pre_full = reinterpret_cast<int*>(smem + C::kOffPrefix);     // [batch + 1]
+    int* pre_part = pre_full + (kMaxPersistentBatch + 1);             // [batch + 1]
+    Item* desc = reinterpret_cast<Item*>(smem + C::kOffDesc);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* empty = full + NSTAGES;
+    uint64_t* item_full = empty + NSTAGES;
+    uint64_t* item_empty = item_full + kQueue;
+    int* abort_flag = reinterpret_cast<int*>(smem + C::kOffFlags);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int n_grp = a.num_kv_heads * n_hg;
+    const int P = a.partition_size;
+    int* sched = a.sched;          // [0]: next item, [1]: CTAs done
+
+    pdl_wait();      // inputs may come from the previous kernel in the stream
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGES; ++i) {
+            mbar_init(smem_addr(full + i), 1);
+            mbar_init(smem_addr(empty + i), 1);
+        }
+        for (int i = 0; i < kQueue; ++i) {
+            mbar_init(smem_addr(item_full + i), 1);
+            mbar_init(smem_addr(item_empty + i), 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kHeadsPerCta * kMergeStride; i += blockDim.x) acc[i] = 0.f;
+    __syncthreads();
+
+    if (warp == kConsumers) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        // prefix sums over the batch: full partitions, and "has a partial one"
+        // (an empty sequence counts as one partial partition: it writes zeros)
+        {
+            const int per = (a.batch + 31) / 32;
+            const int s0 = min(a.batch, lane * per), s1 = min(a.batch, s0 + per);
+            int nf = 0, np = 0;
+            for (int s = s0; s < s1; ++s) {
+                const int c = clamp_ctx(a, s, blockIdx.x == 0);
+                nf += c / P;
+                np += (c % P != 0 || c == 0) ? 1 : 0;
+            }
+            int fi = nf, pi = np;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int fu = __shfl_up_sync(0xffffffffu, fi, off), pu = __shfl_up_sync(0xffffffffu, pi, off);
+                if (lane >= off) { fi += fu; pi += pu; }
+            }
+            int fr = fi - nf, pr = pi - np;
+            for (int s = s0; s < s1; ++s) {
+                const int c = clamp_ctx(a, s, false);
+                pre_full[s] = fr;
+                pre_part[s] = pr;
+                fr += c / P;
+                pr += (c % P != 0 || c == 0) ? 1 : 0;
+            }
+            if (lane == 31) {
+                pre_full[a.batch] = fi;
+                pre_part[a.batch] = pi;
+            }
+            __syncwarp();
+        }
+        const int total_full = pre_full[a.batch];
+        const int total = (total_full + pre_part[a.batch]) * n_grp;
+        const uint64_t policy = l2_evict_first_policy();
+        const int cap = a.max_blocks * BS;
+        // Items are looked ahead: while item n's tiles are issued, the index of
+        // item n+2 is being fetched and item n+1's context length and first 32
+        // block ids are in flight, so no item waits on those round trips.
+        struct Ahead {
+            int idx, s, part, grp, ctx_raw, ids;
+        };
+        auto locate = [&](int idx) {
+            Ahead h{idx, 0, 0, 0, 0, 0};
+            if (idx < total) {
+                int j = idx / n_grp;
+                h.grp = idx - j * n_grp;
+                if (j < total_full) {
+                    h.s = prefix_search(pre_full, a.batch, j);
+                    h.part = j - pre_full[h.s];
+                } else {
+                    j -= total_full;
+                    h.s = prefix_search(pre_part, a.batch, j);
+                    h.part = pre_full[h.s + 1] - pre_full[h.s];
+                }
+                h.ctx_raw = __ldg(a.context_lens + h.s);
+                const int jb = h.part * P / BS + lane;
+                h.ids = jb < a.max_blocks ? __ldg(a.block_tables + static_cast<int64_t>(h.s) * a.max_blocks + jb) : 0;
+            }
+            return h;
+        };
+        int pend = lane == 0 ? atomicAdd(sched, 1) : 0;
+        Ahead cur = locate(__shfl_sync(0xffffffffu, pend, 0));
+        pend = lane == 0 ? atomicAdd(sched, 1) : 0;   // index of the item after `cur`, in flight
+        int k = 0;        // chunks issued (global chunk counter of this CTA)
+        int n = 0;        // items issued
+        bool ok = true;
+        while (ok) {
+            const int slot = n % kQueue;
+            if (n >= kQueue) {
+                int w = 1;
+                if (lane == 0) w = mbar_wait(smem_addr(item_empty + slot), ((n / kQueue) - 1) & 1);
+                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+            }
+            if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = false; break; }
+            if (cur.idx >= total) {   // no work left: tell the consumers
+                if (lane == 0) {
+                    desc[slot].seq = -1;
+                    mbar_arrive(smem_addr(item_full + slot));
+                }
+                break;
+            }
+            const Ahead nxt = locate(__shfl_sync(0xffffffffu, pend, 0));
+            pend = lane == 0 ? atomicAdd(sched, 1) : 0;
+            const int ctx = cur.ctx_raw < 0 ? 0 : min(cur.ctx_raw, cap);
+            Item it;
+            it.seq = cur.s;
+            it.grp = cur.grp;
+            it.part = cur.part;
+            it.tok0 = cur.part * P;
+            it.tok1 = min(ctx, it.tok0 + P);
+            it.chunk0 = k;
+            it.n_chunks = it.tok1 > it.tok0 ? (it.tok1 - it.tok0 + kChunk - 1) / kChunk : 0;
+            it.n_parts = ctx > 0 ? (ctx + P - 1) / P : 1;
+            const int kvh = cur.grp / n_hg;
+            const int h0 = kvh * a.group + (cur.grp - kvh * n_hg) * kHeadsPerCta;
+            const int nh = min(kHeadsPerCta, a.group - (cur.grp - kvh * n_hg) * kHeadsPerCta);
+            if (lane == 0) {
+                desc[slot] = it;
+                const uint32_t fb = smem_addr(item_full + slot);
+                const uint32_t qbytes = nh * kD * 2;
+                mbar_arrive_expect_tx(fb, qbytes);
+                bulk_load(smem_addr(qslots + slot * C::kQSlotBytes),
+                          static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(cur.s) * a.num_q_heads + h0) * kD,
+                          qbytes, fb);
+            }
+            __syncwarp();
+            BlockWindow win;
+            win.start_loaded(a.block_tables + static_cast<int64_t>(cur.s) * a.max_blocks, it.tok0, it.tok1, BS,
+                             cur.ids);
+            for (int c = 0; c < it.n_chunks; ++c) {
+                const int t0 = it.tok0 + c * kChunk;
+                int pb_a, pb_b;
+                win.get(t0, BS, lane, pb_a, pb_b);
+                if (!issue_chunk<C, BS, NSTAGES>(a, &tmap_k, &tmap_v, full, empty, ring, k, lane, kvh, t0, it.tok1,
+                                                 pb_a, pb_b, policy)) {
+                    ok = false;
+                    break;
+                }
+                ++k;
+            }
+            cur = nxt;
+            ++n;
+        }
+        if (!ok && lane == 0) {
+            atomicExch(abort_flag, 1);
+            raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
+        }
+        drain_ring<NSTAGES>(a, full, k, lane);
+    } else {
+        // ------------------------------------------------------ consumers
+        const int tid = threadIdx.x;   // 0..127
+        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale * kFp8WidenScale : 1.f);
+        const float vs = kFp8 ? a.v_scale * kFp8WidenScale : 1.f;
+        Consumer<KV, C> cs;
+        cs.init(lane);
+        for (int n = 0;; ++n) {
+            const int slot = n % kQueue;
+            const bool got = mbar_wait(smem_addr(item_full + slot), (n / kQueue) & 1);
+            // one decision for all consumer warps: stop on a wait that ran out,
+            // here or in an earlier chunk, or on the producer's abort
+            if (consumer_bar_any(!got || *reinterpret_cast<volatile int*>(abort_flag) != 0)) break;
+            const Item it = desc[slot];
+            if (it.seq < 0) break;
+            const int kvh = it.grp / n_hg;
+            const int hg = it.grp - kvh * n_hg;
+            const int h0 = kvh * a.group + hg * kHeadsPerCta;
+            const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
+            cs.reset();
+            cs.template load_q<false>(reinterpret_cast<const uint16_t*>(qslots + slot * C::kQSlotBytes), nh,
+                                      a.q_dtype == PA_BF16);
+            // this warp's chunks: global chunk k belongs to warp k % 4
+            const int first = it.chunk0 + ((warp - it.chunk0) % kConsumers + kConsumers) % kConsumers;
+            for (int k = first; k < it.chunk0 + it.n_chunks; k += kConsumers) {
+                const int st = k % NSTAGES;
+                const bool landed = mbar_wait(smem_addr(full + st), (k / NSTAGES) & 1);
+                if (!__all_sync(0xffffffffu, landed)) {
+                    if (lane == 0) atomicExch(abort_flag, 1);
+                    break;
+                }
+                const uint32_t kb = ring + st * C::kStageBytes;
+                cs.chunk(kb, kb + C::kTileBytes, it.tok1 - (it.tok0 + (k - it.chunk0) * kChunk), sc);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(empty + st));
+            }
+            cs.finish();
+
+            // ---- merge the four warps: each adds its output, rescaled to the
+            // merged per-head maximum, into one shared accumulator
+            if (cs.g == 0) {
+                wm[warp * kHeadsPerCta + 2 * cs.q4] = cs.m0;
+                wm[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.m1;
+                wl[warp * kHeadsPerCta + 2 * cs.q4] = cs.l0;
+                wl[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.l1;
+            }
+            consumer_bar();
+            auto head_max = [&](int h) {
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, wm[w * kHeadsPerCta + h]);
+                return M;
+            };
+            {
+                const int ha = 2 * cs.q4, hb = ha + 1;
+                const float ca = (cs.m0 == kNegInf || ha >= nh) ? 0.f : exp2_approx(cs.m0 - head_max(ha));
+                const float cb = (cs.m1 == kNegInf || hb >= nh) ? 0.f : exp2_approx(cs.m1 - head_max(hb));
+                float* ra = acc + ha * kMergeStride;
+                float* rb = acc + hb * kMergeStride;
+                if (ca != 0.f) {
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        atomicAdd(ra + cs.d_lo(mt), cs.o[mt][0] * ca);
+                        atomicAdd(ra + cs.d_hi(mt), cs.o[mt][2] * ca);
+                    }
+                }
+                if (cb != 0.f) {
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        atomicAdd(rb + cs.d_lo(mt), cs.o[mt][1] * cb);
+                        atomicAdd(rb + cs.d_hi(mt), cs.o[mt][3] * cb);
+                    }
+                }
+            }
+            consumer_bar();
+            // Results, and the accumulator back to zero.  The next item's
+            // start barrier orders these reads before its own adds.
+            for (int i = tid; i < nh * kD; i += kConsumers * 32) {
+                const int h = i / kD, d = i - h * kD;
+                const float M = head_max(h);
+                float L = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w) {
+                    const float mw = wm[w * kHeadsPerCta + h];
+                    L += mw == kNegInf ? 0.f : wl[w * kHeadsPerCta + h] * exp2_approx(mw - M);
+                }
+                const int64_t row = static_cast<int64_t>(it.seq) * a.num_q_heads + h0 + h;
+                store_result(a, row, d, it.part, it.n_parts, L > 0.f ? acc[h * kMergeStride + d] * vs / L : 0.f, M,
+                             L);
+                acc[h * kMergeStride + d] = 0.f;
+            }
+            if (it.n_parts > 1 && a.fused_merge) {
+                merge_group_if_last(a, it.seq, it.seq * n_grp + it.grp, h0, nh, it.n_parts, tid, kConsumers * 32,
+                                    [] { consumer_bar(); });
+            }
+            // the query slot and descriptor were read before the first merge barrier
+            if (tid == 0) mbar_arrive(smem_addr(item_empty + slot));
+        }
+    }
+
+    __syncthreads();
+    // the last CTA to finish resets the item counter for the next call
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+            sched[0] = 0;
+            sched[1] = 0;
+        }
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -461,8 +960,10 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D view of a pool: rows of head_dim elements, one row per (block, head, slot).
-bool make_pool_map(CUtensorMap* map, const void* pool, const DecodeArgs& a, int box_rows) {
+// 2-D view of a pool: rows of head_dim elements, one row per (block, head,
+// slot).  With `three_d`, a 3-D view (64 elements, rows, 2 column halves)
+// whose box covers a whole 16-row tile.
+bool make_pool_map(CUtensorMap* map, const void* pool, const DecodeArgs& a, int box_rows, bool three_d) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const int eb = static_cast<int>(pa_dtype_size(a.kv_dtype));
@@ -473,7 +974,16 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const DecodeArgs& a, int 
                           static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * eb};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (three_d) {
+        cuuint64_t dims3[3] = {static_cast<cuuint64_t>(128 / eb), dims[1], 2};
+        cuuint64_t strides3[2] = {static_cast<cuuint64_t>(kD) * eb, 128};
+        cuuint32_t box3[3] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows), 2};
+        CUresult r = enc(map, t, 3, const_cast<void*>(pool), dims3, strides3, box3, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return r == CUDA_SUCCESS;
+    }
     CUresult r = enc(map, t, 2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -482,18 +992,37 @@ bool make_pool_map(CUtensorMap* map, const void* pool, const DecodeArgs& a, int 
 
 template <pa_dtype KV, int BS, int NSTAGES>
 pa_status launch(const DecodeArgs& a, cudaStream_t stream) {
-    using C = Cfg<KV, BS, NSTAGES>;
-    auto kernel = decode_mma_kernel<KV, BS, NSTAGES>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return PA_ERR_CUDA;
     CUtensorMap mk, mv;
-    if (!make_pool_map(&mk, a.k_cache, a, C::kBoxRows) || !make_pool_map(&mv, a.v_cache, a, C::kBoxRows))
+    constexpr int box_rows = Cfg<KV, BS, NSTAGES>::kBoxRows;
+    constexpr bool three_d = Cfg<KV, BS, NSTAGES>::k3D;
+    if (!make_pool_map(&mk, a.k_cache, a, box_rows, three_d) || !make_pool_map(&mv, a.v_cache, a, box_rows, three_d))
         return PA_ERR_CUDA;
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
+    if (a.persistent) {
+        using C = PersistCfg<KV, BS, NSTAGES>;
+        auto kernel = decode_mma_persistent_kernel<KV, BS, NSTAGES>;
+        // once per instantiation: raise its shared-memory limit, count resident CTAs per SM
+        static std::once_flag once;
+        static cudaError_t err = cudaSuccess;
+        static int per_sm = 0;
+        std::call_once(once, [&] {
+            err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, C::kSmemBytes);
+        });
+        if (err != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
+        const int64_t items = static_cast<int64_t>(a.batch) * a.num_kv_heads * n_hg * a.max_parts;
+        const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(per_sm) * sm_count())));
+        if (launch_pdl(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess)
+            return PA_ERR_CUDA;
+        return PA_OK;
+    }
+    using C = GridCfg<KV, BS, NSTAGES>;
+    auto kernel = decode_mma_kernel<KV, BS, NSTAGES>;
+    static std::once_flag once;   // once per instantiation
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [&] { err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes); });
+    if (err != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(a.max_parts, a.num_kv_heads * n_hg, a.batch);
     if (launch_pdl(kernel, grid, dim3(kThreads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;

@@ -58,11 +58,11 @@ extern "C" pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, con
     if (need > 0 && q && k_cache && v_cache && block_tables && context_lens && out) {
         pa_status st = scratch_address(&ws);
         if (st != PA_OK) return st;
-        // The array keeps the previous call's contents.  Its front holds one
-        // merge counter per (sequence, KV head, head group), which must start
-        // at zero: clear them on the caller's stream, ahead of the kernels.
-        const int64_t groups = (num_q_heads / cache->num_kv_heads + pa::kHeadsPerCta - 1) / pa::kHeadsPerCta;
-        const size_t counters = static_cast<size_t>(batch) * cache->num_kv_heads * groups * sizeof(int32_t);
+        // The array keeps the previous call's contents.  Its front holds the
+        // counters a call expects at zero (work scheduling and merge tickets):
+        // clear them on the caller's stream, ahead of the kernels.
+        const size_t counters =
+            pa::decode_counter_bytes(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
         if (cudaMemsetAsync(ws, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PA_ERR_CUDA;
     }
     return pa_decode_attention(cache, q, q_dtype, num_q_heads, k_cache, v_cache, block_tables, max_blocks_per_seq,

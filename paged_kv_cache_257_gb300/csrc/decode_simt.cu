@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
             }
         }
     }
-    if (n_parts > 1 && a.fused_merge) merge_if_last(a, seq, h0, nh, n_parts);
+    if (n_parts > 1 && a.fused_merge)
+        merge_group_if_last(a, seq, seq * gridDim.y + blockIdx.y, h0, nh, n_parts, threadIdx.x, blockDim.x,
+                            [] { __syncthreads(); });
 }
 
 template <pa_dtype KV, int D>
