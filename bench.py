@@ -139,6 +139,9 @@ class GpuWorkload:
         bs = w.block_size
         self.alloc_tables(wl)
         ctx = self.ctx_decode
+        # 0 = the library plans it from the batch's context lengths, which a
+        # serving host knows when it builds the block tables
+        self.plan = self.partition == 0
         # source values of every cached token (in the cache's source type)
         k_scale = v_scale = 1.0
         seqs_k, seqs_v = [], []
@@ -190,6 +193,9 @@ class GpuWorkload:
             self.q = torch.from_numpy(q).to(device)
         self.block_tables = torch.from_numpy(self.tables_np).to(device)
         self.context_lens = torch.from_numpy(ctx.astype(np.int32)).to(device)
+        self.ctx_host = ctx.astype(np.int32)
+        if self.plan:
+            self.partition = self.plan_partition()
         self.new_k, self.new_v, self.new_slots = self.step_append_inputs(wl, dev)
         self.workspace = None
         need = pa.decode_workspace_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], self.partition)
@@ -211,6 +217,10 @@ class GpuWorkload:
         self.allocator = self.pa.BlockAllocator(w.num_blocks, w.alloc_seed)
         self.tables_np, self.ctx_decode, self.append_slots = wl.build_prefix_tables(w, self.allocator)
         self.append_positions = w.context_lens.copy()
+
+    def plan_partition(self):
+        w = self.w
+        return self.pa.plan_partition(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], self.ctx_host)
 
     def step_append_inputs(self, wl, dev):
         torch = self.torch
@@ -292,8 +302,9 @@ def time_e2e(wk, steps, warmup):
         kc, vc = wk.pools[r % len(wk.pools)]
         if "k" in dev:
             pa.kv_append(wk.desc, dev["k"], dev["v"], dev["slots"], kc, vc)
+        part = wk.plan_partition() if wk.plan else wk.partition   # host work of a serving step
         pa.decode_attention(wk.desc, dev["q"], kc, vc, dev["bt"], dev["ctx"], wk.w.scale,
-                            partition=wk.partition, workspace=wk.workspace, out=wk.out)
+                            partition=part, workspace=wk.workspace, out=wk.out)
         out_host.copy_(wk.out, non_blocking=True)
 
     for i in range(warmup):

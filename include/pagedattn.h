@@ -157,8 +157,9 @@ pa_status pa_copy_blocks(const pa_cache_desc* cache, void* k_cache, void* v_cach
 
 /* Tokens per split-context partition the library uses for this problem:
  * `requested` > 0 is checked (a multiple of 16 and of block_size) and
- * returned; 0 picks one from the shape; -1 means one partition covering
- * max_blocks_per_seq*block_size tokens.  Returns -1 on invalid input. */
+ * returned; 0 picks one as pa_decode_plan_partition does with every
+ * sequence at max_blocks_per_seq*block_size tokens; -1 means one partition
+ * covering that many tokens.  Returns -1 on invalid input. */
 int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                  int32_t max_blocks_per_seq, int32_t requested);
 
@@ -168,6 +169,22 @@ int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int3
  * for invalid input.  The workspace must be zero-filled before its first
  * use; every completed call leaves its counters at zero again, so one
  * zeroed buffer serves any sequence of calls that are not concurrent. */
+/* Partition size for a batch whose context lengths the host knows (a
+ * serving loop knows them: it built the block tables).  The pages do not
+ * size partitions; this models a call as waves of work items (one per
+ * partition, sequence and group of up to 8 query heads) over the resident
+ * CTAs, each wave as long as its longest item plus a fixed per-item cost,
+ * and returns the candidate (the whole context, 8192 ... 256 tokens) with
+ * the least modelled time.  Pass the result as pa_decode_attention's
+ * partition_size with the same cache, batch, num_q_heads and
+ * max_blocks_per_seq.
+ *   host_context_lens  host [batch] int32 (null: every sequence full)
+ *   num_sms            SMs to plan for; <= 0 asks the current device
+ * Returns -1 on invalid input or when num_sms <= 0 and no device answers. */
+int32_t pa_decode_plan_partition(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                 int32_t max_blocks_per_seq, const int32_t* host_context_lens,
+                                 int32_t num_sms);
+
 size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                 int32_t max_blocks_per_seq, int32_t partition_size);
 

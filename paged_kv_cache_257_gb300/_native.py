@@ -46,6 +46,7 @@ SIGNATURES = {
     "pa_copy_blocks": (ctypes.c_int, [P_desc, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p,
                                       c_void_p]),
     "pa_decode_partition_size": (c_int32, [P_desc, c_int32, c_int32, c_int32, c_int32]),
+    "pa_decode_plan_partition": (c_int32, [P_desc, c_int32, c_int32, c_int32, c_void_p, c_int32]),
     "pa_decode_workspace_size": (c_size_t, [P_desc, c_int32, c_int32, c_int32, c_int32]),
     "pa_decode_attention": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p, c_void_p,
                                            c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p, c_size_t,

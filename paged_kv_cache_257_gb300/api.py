@@ -130,6 +130,23 @@ def partition_size(desc, batch, num_q_heads, max_blocks_per_seq, requested=0):
     return int(lib().pa_decode_partition_size(ctypes.byref(c), batch, num_q_heads, max_blocks_per_seq, requested))
 
 
+def plan_partition(desc, batch, num_q_heads, max_blocks_per_seq, context_lens=None, num_sms=0):
+    """Partition size for a batch whose context lengths are known on the host
+    (``context_lens``: host int sequence, or None for every sequence full);
+    ``num_sms`` <= 0 asks the current device."""
+    c = desc.c()
+    arr = None
+    if context_lens is not None:
+        arr = np.ascontiguousarray(np.asarray(context_lens), dtype=np.int32)
+        if arr.shape != (batch,):
+            raise ValueError(f"context_lens must hold {batch} lengths, got shape {arr.shape}")
+    p = int(lib().pa_decode_plan_partition(ctypes.byref(c), batch, num_q_heads, max_blocks_per_seq,
+                                           None if arr is None else arr.ctypes.data, num_sms))
+    if p <= 0:
+        raise ValueError("pa_decode_plan_partition rejected its arguments")
+    return p
+
+
 def decode_workspace_size(desc, batch, num_q_heads, max_blocks_per_seq, partition=0):
     c = desc.c()
     return int(lib().pa_decode_workspace_size(ctypes.byref(c), batch, num_q_heads, max_blocks_per_seq, partition))
@@ -301,5 +318,5 @@ class BlockAllocator:
 
 
 __all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
-           "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size",
+           "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size", "plan_partition",
            "decode_workspace_size", "decode_attention", "decode_attention_noalloc", "new_status", "new_workspace", "read_device_status"]

@@ -36,6 +36,12 @@ struct DecodeArgs {
 // Query heads one CTA serves (a KV head's group is split into chunks of this).
 constexpr int kHeadsPerCta = 8;
 
+// CTAs of the tensor-core decode kernel resident per SM (its register budget
+// is sized for this many).
+#ifndef PA_DECODE_MIN_CTAS
+#define PA_DECODE_MIN_CTAS 5
+#endif
+
 // Up to this many partitions per sequence the decode kernel merges them itself.
 constexpr int kFusedMergeMaxParts = 16;
 

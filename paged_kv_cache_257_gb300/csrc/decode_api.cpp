@@ -43,21 +43,54 @@ bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p
 // Tokens per partition must be a multiple of the 16-token chunk and of the block size.
 int32_t partition_unit(int32_t block_size) { return std::max(16, block_size); }
 
-// Auto choice: the largest partition (fewer partials to merge) that still
-// gives a few waves of CTAs even when only part of the batch is long.
-int32_t auto_partition(const pa_cache_desc* c, int32_t batch, int32_t num_q_heads, int64_t cap) {
+// Partition planning.  A work item (one CTA) covers one partition of one
+// sequence for one group of query heads; the resident CTAs stream the KV
+// cache at a shared rate, so a call takes about
+//     waves x (tokens of the longest item + kItemOverheadTokens)
+// with waves = ceil(items / resident CTAs).  The overhead stands for what an
+// item costs beyond its tokens (filling and draining its pipeline, writing
+// and merging a partial); 192 tokens matches the partition sweeps of the
+// tensor-core kernel on GB300 (Llama-3-8B ragged batch, 13B MHA, 70B 128k FP8).
+constexpr int64_t kItemOverheadTokens = 192;
+
+int64_t plan_cost(int64_t items, int64_t longest_item, int64_t slots) {
+    const int64_t waves = std::max<int64_t>(1, (items + slots - 1) / slots);
+    return waves * (longest_item + kItemOverheadTokens);
+}
+
+// The partition with the least modelled time, from the whole context down to
+// 256 tokens; ties go to the larger partition (fewer partials).  `lens` holds
+// the batch's context lengths, or is null to assume every sequence at `cap`.
+int32_t plan_partition(const pa_cache_desc* c, int32_t batch, int32_t num_q_heads, int64_t cap,
+                       const int32_t* lens, int32_t num_sms) {
     const int32_t unit = partition_unit(c->block_size);
     const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
-    const int64_t units = static_cast<int64_t>(batch) * c->num_kv_heads * groups;
-    const int64_t want = 16ll * sm_count();
-    const int64_t whole = (cap + unit - 1) / unit * unit;
-    if (units >= want) return static_cast<int32_t>(std::max<int64_t>(whole, unit));
+    const int64_t per_seq = static_cast<int64_t>(c->num_kv_heads) * groups;
+    const int64_t slots = static_cast<int64_t>(PA_DECODE_MIN_CTAS) * std::max(num_sms, 1);
+    const int64_t whole = std::max<int64_t>((cap + unit - 1) / unit * unit, unit);
+    int64_t longest = 0;
+    for (int32_t s = 0; s < batch; ++s)
+        longest = std::max<int64_t>(longest, lens ? std::min<int64_t>(std::max(lens[s], 0), cap) : cap);
+    auto items_for = [&](int64_t p) {
+        int64_t n = 0;
+        for (int32_t s = 0; s < batch; ++s) {
+            const int64_t ctx = lens ? std::min<int64_t>(std::max(lens[s], 0), cap) : cap;
+            n += (ctx + p - 1) / p;
+        }
+        return n * per_seq;
+    };
+    int64_t best = whole;
+    int64_t best_cost = plan_cost(items_for(whole), std::min(whole, longest), slots);
     const int32_t cands[] = {8192, 4096, 2048, 1024, 512, 256};
     for (int32_t p : cands) {
         if (p % unit != 0 || p >= whole) continue;
-        if (units * ((cap + p - 1) / p) >= want) return p;
+        const int64_t cost = plan_cost(items_for(p), std::min<int64_t>(p, longest), slots);
+        if (cost < best_cost) {
+            best = p;
+            best_cost = cost;
+        }
     }
-    return std::min<int32_t>(256, static_cast<int32_t>(std::max<int64_t>(whole, unit)));
+    return static_cast<int32_t>(best);
 }
 
 }  // namespace
@@ -75,8 +108,21 @@ extern "C" int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t 
     if (cap >= (int64_t{1} << 31)) return -1;
     if (requested == -1) return static_cast<int32_t>((cap + unit - 1) / unit * unit);
     if (requested > 0) return requested % unit == 0 ? requested : -1;
-    if (requested == 0) return auto_partition(cache, batch, num_q_heads, cap);
+    if (requested == 0) return plan_partition(cache, batch, num_q_heads, cap, nullptr, sm_count());
     return -1;
+}
+
+extern "C" int32_t pa_decode_plan_partition(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
+                                            int32_t max_blocks_per_seq, const int32_t* host_context_lens,
+                                            int32_t num_sms) {
+    if (check_cache_desc(cache) != PA_OK || batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+        num_q_heads % cache->num_kv_heads != 0)
+        return -1;
+    const int64_t cap = static_cast<int64_t>(max_blocks_per_seq) * cache->block_size;
+    if (cap >= (int64_t{1} << 31)) return -1;
+    if (num_sms <= 0) num_sms = sm_count();
+    if (num_sms <= 0) return -1;
+    return plan_partition(cache, batch, num_q_heads, cap, host_context_lens, num_sms);
 }
 
 namespace pa {

@@ -454,7 +454,7 @@ struct GridCfg : Cfg<KV, BS, NSTAGES> {
 };
 
 template <pa_dtype KV, int BS, int NSTAGES>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_CTAS)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeArgs a) {
     using C = GridCfg<KV, BS, NSTAGES>;

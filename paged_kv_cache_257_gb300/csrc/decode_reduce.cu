@@ -16,36 +16,46 @@
 namespace pa {
 namespace {
 
-constexpr int kWarps = 8;
+#ifndef PA_REDUCE_WARPS
+#define PA_REDUCE_WARPS 16
+#endif
+constexpr int kWarps = PA_REDUCE_WARPS;
 constexpr int kThreads = kWarps * 32;
-constexpr int kUnroll = 8;   // independent partial loads in flight per lane
+constexpr int kUnroll = 8;   // partitions in flight per warp
 constexpr float kNegInf = -__builtin_huge_valf();
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* scratch) {
+// head_dim / 32 consecutive floats of a partial row: one vector load.
+template <int N>
+struct Slice {
+    float v[N];
+    __device__ __forceinline__ void load(const float* p) {
+        if constexpr (N == 2) {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(p));
+            v[0] = t.x; v[1] = t.y;
+        } else {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, v, off);
-        v = is_max ? fmaxf(v, o) : v + o;
+            for (int i = 0; i < N; i += 4) {
+                const float4 t = __ldcg(reinterpret_cast<const float4*>(p + i));
+                v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+            }
+        }
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    float r = scratch[0];
-    for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, scratch[w]) : r + scratch[w];
-    __syncthreads();
-    return r;
-}
+};
 
-// One CTA per (query head, sequence, 32-wide slice of head_dim).  Warp w sums
-// partitions w, w+8, ... for the 32 output elements (one per lane, coalesced
-// 128-byte rows), kUnroll loads at a time; the 8 warp sums meet in shared memory.
+// One CTA per (query head, sequence).  Every warp takes the maximum of all
+// m_p itself, so no barrier precedes the sums; warp w then adds partitions
+// w, w+kWarps, ..., kUnroll of them in flight, lane j holding d = j*D/32 ..
+// (j+1)*D/32 - 1 of each partial row (one coalesced row per partition).  The
+// weights are the same in every lane, so each lane keeps the warp's weight
+// sum; the warps' sums meet in shared memory behind one barrier.
+template <int D>
 __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArgs a) {
-    extern __shared__ float weights[];
-    __shared__ float scratch[kWarps];
-    __shared__ float sums[kWarps][32];
+    constexpr int kVec = D / 32;
+    __shared__ __align__(16) float s_acc[kWarps][D];
+    __shared__ float s_l[kWarps];
     const int hq = blockIdx.x, seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    pdl_wait();      // inputs may come from the previous kernel in the stream
+    pdl_wait();      // the partials come from the previous kernel in the stream
     pdl_trigger();
     int ctx = __ldg(a.context_lens + seq);
     const int cap = a.max_blocks * a.block_size;
@@ -53,59 +63,69 @@ __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArg
     const int n_parts = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 1;
     if (n_parts <= 1) return;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + hq;
-    const float* ml = a.part_ml + row * a.max_parts * 2;
-    const int d = blockIdx.z * 32 + lane;
-    const float* po = a.part_o + row * a.max_parts * a.head_dim + d;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml + row * a.max_parts * 2);
+    const float* po = a.part_o + row * a.max_parts * D + lane * kVec;
 
     float M = kNegInf;
-    for (int p = threadIdx.x; p < n_parts; p += kThreads) M = fmaxf(M, ml[2 * p]);
-    M = block_reduce(M, true, scratch);
-    float L = 0.f;
-    for (int p = threadIdx.x; p < n_parts; p += kThreads) {
-        const float mp = ml[2 * p];
-        const float w = mp == kNegInf ? 0.f : ml[2 * p + 1] * exp2_approx(mp - M);
-        weights[p] = w;
-        L += w;
-    }
-    L = block_reduce(L, false, scratch);  // its barriers also publish `weights`
-
-    float acc[kUnroll];
+#pragma unroll 4
+    for (int p = lane; p < n_parts; p += 32) M = fmaxf(M, __ldcg(ml + p).x);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) acc[u] = 0.f;
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+    float acc[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
+    float L = 0.f;
+    auto add = [&](const float2 mlp, const Slice<kVec>& o) {
+        const float w = mlp.x == kNegInf ? 0.f : mlp.y * exp2_approx(mlp.x - M);
+        L += w;
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(w, o.v[i], acc[i]);
+    };
     int p = warp;
     for (; p + (kUnroll - 1) * kWarps < n_parts; p += kUnroll * kWarps) {
-        float v[kUnroll];
+        float2 mlp[kUnroll];
+        Slice<kVec> o[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = po[static_cast<int64_t>(p + u * kWarps) * a.head_dim];
+        for (int u = 0; u < kUnroll; ++u) {
+            mlp[u] = __ldcg(ml + p + u * kWarps);
+            o[u].load(po + static_cast<int64_t>(p + u * kWarps) * D);
+        }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) acc[u] = fmaf(weights[p + u * kWarps], v[u], acc[u]);
+        for (int u = 0; u < kUnroll; ++u) add(mlp[u], o[u]);
     }
-    for (; p < n_parts; p += kWarps) acc[0] = fmaf(weights[p], po[static_cast<int64_t>(p) * a.head_dim], acc[0]);
-    float sum = 0.f;
+    for (; p < n_parts; p += kWarps) {
+        Slice<kVec> o;
+        o.load(po + static_cast<int64_t>(p) * D);
+        add(__ldcg(ml + p), o);
+    }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) sum += acc[u];
-    sums[warp][lane] = sum;
+    for (int i = 0; i < kVec; ++i) s_acc[warp][lane * kVec + i] = acc[i];
+    if (lane == 0) s_l[warp] = L;
     __syncthreads();
-    if (warp == 0) {
+    float lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) lt += s_l[w];
+    for (int d = threadIdx.x; d < D; d += kThreads) {
         float t = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += sums[w][lane];
-        store_out(a.out, row * a.head_dim + d, L > 0.f ? t / L : 0.f, a.out_dtype);
+        for (int w = 0; w < kWarps; ++w) t += s_acc[w][d];
+        store_out(a.out, row * D + d, lt > 0.f ? t / lt : 0.f, a.out_dtype);
     }
 }
 
 }  // namespace
 
 pa_status launch_decode_reduce(const DecodeArgs& a, cudaStream_t stream) {
-    const int smem = a.max_parts * static_cast<int>(sizeof(float));
-    if (smem > 48 * 1024) {
-        static cudaError_t err = cudaFuncSetAttribute(decode_reduce_kernel,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-        if (err != cudaSuccess) return PA_ERR_CUDA;
+    const dim3 grid(a.num_q_heads, a.batch);
+    cudaError_t err;
+    switch (a.head_dim) {
+        case 64: err = launch_pdl(decode_reduce_kernel<64>, grid, dim3(kThreads), 0, stream, a); break;
+        case 128: err = launch_pdl(decode_reduce_kernel<128>, grid, dim3(kThreads), 0, stream, a); break;
+        case 256: err = launch_pdl(decode_reduce_kernel<256>, grid, dim3(kThreads), 0, stream, a); break;
+        default: return PA_ERR_UNSUPPORTED;
     }
-    dim3 grid(a.num_q_heads, a.batch, a.head_dim / 32);
-    if (launch_pdl(decode_reduce_kernel, grid, dim3(kThreads), smem, stream, a) != cudaSuccess) return PA_ERR_CUDA;
-    return PA_OK;
+    return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace pa

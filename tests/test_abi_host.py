@@ -219,3 +219,40 @@ def test_workspace_and_partition_sizes(pa):
     assert pa.partition_size(d, 4, 64, 8192, 100) == -1
     auto = pa.partition_size(d, 4, 64, 8192, 0)
     assert auto > 0 and auto % 16 == 0
+
+
+def test_plan_partition_follows_the_wave_model(pa):
+    """Costs worked by hand: waves = ceil(items / (5 x 152)), each as long as
+    its longest item plus 192 tokens; ties keep the larger partition."""
+    gqa = pa.CacheDesc(8192, 16, 8, 128, "bf16", 1.0, 1.0)
+    # 32 full 4096-token sequences, 8 KV heads: 4096 -> 1 x 4288, 2048 -> 1 x 2240,
+    # 1024 -> 2 x 1216, 512 -> 3 x 704 = 2112 (least), 256 -> 6 x 448
+    assert pa.plan_partition(gqa, 32, 32, 256, [4096] * 32, 152) == 512
+    # the same batch at 1024 tokens each: 512 -> 1 x 704 beats 256 -> 2 x 448 and the whole 1 x 1216
+    assert pa.plan_partition(gqa, 32, 32, 256, [1024] * 32, 152) == 512
+    # one short sequence: every candidate costs 100 + 192; the whole context wins the tie
+    assert pa.plan_partition(gqa, 1, 32, 256, [100], 152) == 4096
+    # unknown lengths are taken as full
+    assert pa.plan_partition(gqa, 32, 32, 256, None, 152) == 512
+    fp8 = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
+    # 4 x 131072 tokens, 64 query heads (one group of 8 per KV head): 2048 -> 3 x 2240
+    # beats 1024 -> 6 x 1216, 512 -> 11 x 704 and 4096 -> 2 x 4288
+    assert pa.plan_partition(fp8, 4, 64, 8192, [131072] * 4, 152) == 2048
+    # a ragged batch plans from its real lengths: one long sequence among short
+    # ones is cut finest, as all its pieces still fit one wave:
+    # 256 -> (16 + 31 x 2) x 8 = 624 items, 1 x (256 + 192) beats 512 -> 1 x 704
+    assert pa.plan_partition(gqa, 32, 32, 256, [4096] + [300] * 31, 152) == 256
+    # ... and not when the batch is long as a whole (the full case above gives 512)
+    assert pa.plan_partition(gqa, 32, 32, 256, [4096] * 31 + [300], 152) == 512
+    bs32 = pa.CacheDesc(4096, 32, 8, 128, "bf16", 1.0, 1.0)
+    assert pa.plan_partition(bs32, 32, 32, 128, [4096] * 32, 152) % 32 == 0
+
+
+def test_plan_partition_rejects_bad_arguments(pa):
+    d = pa.CacheDesc(8192, 16, 8, 128, "bf16", 1.0, 1.0)
+    with pytest.raises(ValueError):
+        pa.plan_partition(d, 4, 32, 256, [1, 2, 3], 152)     # 3 lengths for 4 sequences
+    with pytest.raises(ValueError):
+        pa.plan_partition(d, 4, 30, 256, [1] * 4, 152)       # 30 query heads over 8 KV heads
+    # partition_size's automatic choice is the plan for full sequences on this device
+    assert pa.partition_size(d, 4, 32, 256, 0) == pa.plan_partition(d, 4, 32, 256, None, 0)
