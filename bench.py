@@ -252,6 +252,27 @@ class GpuWorkload:
         return n + 1 + (1 if self.workspace is not None else 0)
 
 
+# DRAM bytes (read + write) of one decode_mma_kernel launch, from the ncu
+# captures summarised in profiles/decode_mma_<workload>.md.  They hold for the
+# kernel sources they were taken on (first 16 hex digits of the sha256 of the
+# files below, concatenated); after any change to them traffic is reported as
+# null until a new capture is recorded here.
+TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
+                   "paged_kv_cache_257_gb300/csrc/decode.h")
+NCU_TRAFFIC = {"c9b85a47c54a9db1": {"gqa_bf16": 283_139_840 + 3_936_512,
+                                    "longctx_fp8": 1_074_026_000 + 8_757_760}}
+
+
+def captured_traffic(workload):
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    return NCU_TRAFFIC.get(h.hexdigest()[:16], {}).get(workload)
+
+
 def time_device(wk, steps, warmup, probe_s=0.0):
     """Timed region: barrier + synchronize, K steps, synchronize; per-decode events too.
 
@@ -455,7 +476,8 @@ def main():
         "kv_gbs": wk.kv_bytes * world / step_s / 1e9,
         "decode_kernel_us": dec_avg_s * 1e6,
         "roofline": {"bound": "hbm", "kernel": "paged decode (decode + split merge)", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": captured_traffic(args.workload), "traffic_of": "one decode_mma_kernel launch (ncu)",
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
