@@ -174,6 +174,43 @@ class BlockAllocator:
         for b in table_row[:num_blocks]:
             self.decref(b)
 
+    def truncate(self, table_row, num_blocks, start, length, keep, block_size):
+        """Slide a sequence's window so that only its last ``keep`` tokens stay.
+
+        [VK] "PagedAttention: the idea": when the window slides, the oldest
+        page goes back to the allocator.  [VK] "A minimal PyTorch sketch",
+        ``truncate`` and the notes under it: whole pages are dropped first and
+        what remains of the drop is an offset into the first kept page, with
+        no copy.  The sketch records that offset only by shortening the
+        length, which would make later reads return the wrong rows; the
+        reading taken here keeps an explicit start instead.
+
+        The sequence occupies row positions ``[start, length)`` (position p
+        in ``table_row[p // block_size]``, offset ``p % block_size``).  The
+        new start is ``max(start, length - keep)``; every block whose
+        positions all lie before it is released (``decref``, row order) and
+        removed from the front of the row, the remaining ids move to the
+        front and the freed tail entries become -1.  Positions then count
+        from the first remaining block.  Returns ``(num_blocks, start,
+        length)``.  All or nothing: bad arguments or ids change no state.
+        """
+        if keep < 0 or start < 0 or start > length or length > num_blocks * block_size \
+                or num_blocks > len(table_row):
+            raise AllocError("RANGE", "bad window")
+        new_start = max(start, length - keep)
+        drop = new_start // block_size
+        uses = {}
+        for b in table_row[:drop]:
+            self._check_id(b)
+            uses[b] = uses.get(b, 0) + 1
+            if self.ref[b] < uses[b]:
+                raise AllocError("INVALID", f"block {b} over-released")
+        for b in table_row[:drop]:
+            self.decref(b)
+        kept = list(table_row[drop:num_blocks])
+        table_row[:num_blocks] = kept + [-1] * drop
+        return num_blocks - drop, new_start - drop * block_size, length - drop * block_size
+
     # -- state -----------------------------------------------------------
     @property
     def free_count(self):

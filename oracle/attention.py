@@ -47,7 +47,7 @@ def decode_attention_contiguous(q, K, V, scale):
 
 
 def decode_attention_paged(q, k_pool, v_pool, block_tables, context_lens, scale,
-                           kv_dtype, k_scale=1.0, v_scale=1.0, q_dtype="f32"):
+                           kv_dtype, k_scale=1.0, v_scale=1.0, q_dtype="f32", context_starts=None):
     """Output ``[batch, n_q_heads, head_dim]`` (float64) of paged decode attention.
 
     [DEV] section 4 "The PagedAttention CUDA Kernel": for each sequence the
@@ -55,15 +55,19 @@ def decode_attention_paged(q, k_pool, v_pool, block_tables, context_lens, scale,
     and fetches K and V from the scattered physical blocks.  Here that is the
     logical gather of ``oracle.cache.gather_logical`` followed by the
     contiguous definition above, on the exactly dequantised cache values
-    (``decode(code) * scale`` for FP8).
+    (``decode(code) * scale`` for FP8).  ``context_starts`` (one per
+    sequence, default 0) restricts sequence s to the positions
+    ``context_starts[s] .. context_lens[s] - 1`` of its row: a window slid by
+    truncation ([VK] "A minimal PyTorch sketch"); an empty window gives 0.
     """
     qf = numerics.to_f64(q, q_dtype)
     batch = qf.shape[0]
     out = np.zeros(qf.shape, dtype=np.float64)
     for s in range(batch):
         ctx = int(context_lens[s])
-        Kr = cache.gather_logical(k_pool, block_tables[s], ctx)
-        Vr = cache.gather_logical(v_pool, block_tables[s], ctx)
+        st = 0 if context_starts is None else min(int(context_starts[s]), ctx)
+        Kr = cache.gather_logical(k_pool, block_tables[s], ctx, st)
+        Vr = cache.gather_logical(v_pool, block_tables[s], ctx, st)
         K = numerics.to_f64(Kr, kv_dtype, k_scale)
         V = numerics.to_f64(Vr, kv_dtype, v_scale)
         out[s] = decode_attention_contiguous(qf[s], K, V, scale)

@@ -66,16 +66,19 @@ def kv_append(k_pool, v_pool, k, v, slots, src_dtype, cache_dtype,
         v_pool[b, :, off, :] = vq[t]
 
 
-def gather_logical(pool, block_table_row, context_len):
-    """Logical ``[context_len, n_kv_heads, head_dim]`` view of one sequence.
+def gather_logical(pool, block_table_row, context_len, start=0):
+    """Logical ``[context_len - start, n_kv_heads, head_dim]`` view of one
+    sequence: its tokens at positions ``start .. context_len - 1``.
 
     [DEV] section 4, block-table diagram: logical block j of a sequence lives
     in physical block ``block_table_row[j]``; walking the table in order
-    recovers the sequence's tokens in order.
+    recovers the sequence's tokens in order.  ``start`` > 0 is a slid window
+    ([VK] "A minimal PyTorch sketch", truncate): positions before it are not
+    read, so their blocks may have been released.
     """
     nb, hkv, bs, d = pool.shape
     rows = []
-    for t in range(int(context_len)):
+    for t in range(int(start), int(context_len)):
         pb = int(block_table_row[t // bs])
         if not 0 <= pb < nb:
             raise ValueError("block id out of range")
