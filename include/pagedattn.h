@@ -223,6 +223,26 @@ pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtyp
                               int32_t partition_size, void* workspace, size_t workspace_bytes,
                               void* out, pa_dtype out_dtype, int32_t* device_status, void* stream);
 
+/* pa_decode_attention over a slid window: sequence s attends only the
+ * positions context_starts[s] .. context_lens[s] - 1 of its block-table row
+ * ([VK] "PagedAttention: the idea" and "A minimal PyTorch sketch",
+ * truncate: after the oldest pages go back to the allocator, the rest of the
+ * drop is an offset into the first kept page; pa_alloc_truncate returns that
+ * start and length).  Blocks wholly before a start are never read, so their
+ * table entries may hold anything.
+ *   context_starts  device [batch] int32 in [0, context_lens[s]], or null
+ *                   (every start 0: the same as pa_decode_attention).  A
+ *                   start outside that range is clamped into it and raises
+ *                   PA_DEVFLAG_CONTEXT_RANGE; an empty window gives a zero row.
+ * Every other argument, the workspace size and the partition size are those
+ * of pa_decode_attention. */
+pa_status pa_decode_attention_window(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                     int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, const int32_t* context_starts, int32_t batch,
+                                     float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                     void* out, pa_dtype out_dtype, int32_t* device_status, void* stream);
+
 /* pa_decode_attention for callers that cannot allocate device memory (the
  * pages have no counterpart: this serves the library's users).  Some callers
  * cannot call cudaMalloc: code inside a host framework or server that owns
@@ -309,6 +329,25 @@ pa_status pa_alloc_append_slot(pa_allocator* a, int32_t* table_row, int32_t capa
 
 /* incref (fork) / decref (free) every block of a row, in row order.  On error
  * the blocks already processed are rolled back. */
+/* Slide a sequence's window so that only its last `keep` tokens stay
+ * ([VK] "PagedAttention: the idea": the oldest page goes back to the
+ * allocator; "A minimal PyTorch sketch", truncate: whole pages first, the
+ * rest of the drop as an offset into the first kept page, no copy).  The
+ * sequence occupies row positions [*start, *length) of `table_row` (host,
+ * `capacity` entries, *num_blocks valid; position p lives in block
+ * table_row[p / block_size] at offset p % block_size).  The new first
+ * position is max(*start, *length - keep); every block wholly before it is
+ * released (decref, row order) and removed from the front of the row, the
+ * remaining ids move to the front and the freed tail entries become -1;
+ * positions then count from the first remaining block, so *start ends below
+ * block_size.  Pass *start and *length as pa_decode_attention_window's
+ * context start and length, and *length as the next append position.
+ * PA_ERR_RANGE for keep < 0 or an inconsistent window or an id out of
+ * range, PA_ERR_INVALID for a block released more often than it is held;
+ * on error nothing changes. */
+pa_status pa_alloc_truncate(pa_allocator* a, int32_t* table_row, int32_t capacity, int32_t* num_blocks,
+                            int32_t* start, int32_t* length, int32_t keep, int32_t block_size);
+
 pa_status pa_alloc_fork(pa_allocator* a, const int32_t* table_row, int32_t num_blocks);
 pa_status pa_alloc_free_sequence(pa_allocator* a, const int32_t* table_row, int32_t num_blocks);
 

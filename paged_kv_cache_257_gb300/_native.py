@@ -51,6 +51,9 @@ SIGNATURES = {
     "pa_decode_attention": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p, c_void_p,
                                            c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p, c_size_t,
                                            c_void_p, ctypes.c_int, c_void_p, c_void_p]),
+    "pa_decode_attention_window": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p,
+                                                  c_void_p, c_int32, c_void_p, c_void_p, c_int32, c_float, c_int32,
+                                                  c_void_p, c_size_t, c_void_p, ctypes.c_int, c_void_p, c_void_p]),
     "pa_decode_attention_noalloc": (ctypes.c_int, [P_desc, c_void_p, ctypes.c_int, c_int32, c_void_p, c_void_p,
                                                    c_void_p, c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p,
                                                    ctypes.c_int, c_void_p, c_void_p]),
@@ -68,6 +71,7 @@ SIGNATURES = {
                                             P_int32, P_int32]),
     "pa_alloc_fork": (ctypes.c_int, [c_void_p, c_void_p, c_int32]),
     "pa_alloc_free_sequence": (ctypes.c_int, [c_void_p, c_void_p, c_int32]),
+    "pa_alloc_truncate": (ctypes.c_int, [c_void_p, c_void_p, c_int32, P_int32, P_int32, P_int32, c_int32, c_int32]),
     "pa_alloc_dump": (ctypes.c_int, [c_void_p, c_void_p, P_int32, c_void_p]),
 }
 

@@ -153,16 +153,22 @@ def decode_workspace_size(desc, batch, num_q_heads, max_blocks_per_seq, partitio
 
 
 def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scale, partition=0, workspace=None,
-                     out=None, out_dtype=None, status=None, stream=None):
+                     out=None, out_dtype=None, status=None, stream=None, context_starts=None):
     """Single-query paged decode attention (``pa_decode_attention``); returns ``out``.
 
     ``q`` is ``[batch, num_q_heads, head_dim]``; ``block_tables`` int32
     ``[batch, max_blocks]``; ``context_lens`` int32 ``[batch]``.  ``out`` and
     the split-context ``workspace`` are allocated with torch when not given.
+    ``context_starts`` (device int32 ``[batch]``) restricts each sequence to
+    the positions from its start on (``pa_decode_attention_window``).
     """
     _need(q, "q")
     _need(block_tables, "block_tables", torch.int32)
     _need(context_lens, "context_lens", torch.int32)
+    if context_starts is not None:
+        _need(context_starts, "context_starts", torch.int32)
+        if context_starts.shape != context_lens.shape:
+            raise ValueError("context_starts must have the shape of context_lens")
     batch, hq, d = q.shape
     max_blocks = block_tables.shape[1]
     if out is None:
@@ -174,11 +180,19 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = new_workspace(need, q.device)
     c = desc.c()
-    st = lib().pa_decode_attention(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
-                                   _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
-                                   float(scale), partition, _ptr(workspace) if need else None,
-                                   need if need else 0, _ptr(out), DTYPE[od], _ptr(status), _stream(stream))
-    check("pa_decode_attention", st)
+    if context_starts is None:
+        st = lib().pa_decode_attention(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(block_tables), max_blocks, _ptr(context_lens), batch,
+                                       float(scale), partition, _ptr(workspace) if need else None,
+                                       need if need else 0, _ptr(out), DTYPE[od], _ptr(status), _stream(stream))
+        check("pa_decode_attention", st)
+    else:
+        st = lib().pa_decode_attention_window(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq,
+                                              _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), max_blocks,
+                                              _ptr(context_lens), _ptr(context_starts), batch, float(scale),
+                                              partition, _ptr(workspace) if need else None, need if need else 0,
+                                              _ptr(out), DTYPE[od], _ptr(status), _stream(stream))
+        check("pa_decode_attention_window", st)
     return out
 
 
@@ -296,6 +310,18 @@ class BlockAllocator:
     def free_sequence(self, table_row, num_blocks):
         arr = np.ascontiguousarray(table_row[:num_blocks], dtype=np.int32)
         _alloc_check("pa_alloc_free_sequence", lib().pa_alloc_free_sequence(self._h, arr.ctypes.data, num_blocks))
+
+    def truncate(self, table_row, num_blocks, start, length, keep, block_size):
+        """Keep the last ``keep`` tokens of a sequence (``pa_alloc_truncate``);
+        updates ``table_row`` (a list) in place and returns ``(num_blocks,
+        start, length)``."""
+        arr = (ctypes.c_int32 * len(table_row))(*table_row)
+        n, s0, ln = ctypes.c_int32(num_blocks), ctypes.c_int32(start), ctypes.c_int32(length)
+        st = lib().pa_alloc_truncate(self._h, arr, len(table_row), ctypes.byref(n), ctypes.byref(s0),
+                                     ctypes.byref(ln), keep, block_size)
+        _alloc_check("pa_alloc_truncate", st)
+        table_row[:] = list(arr)
+        return n.value, s0.value, ln.value
 
     @property
     def free_count(self):

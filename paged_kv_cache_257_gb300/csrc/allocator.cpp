@@ -7,6 +7,11 @@
 // blocks under a reference count, and a branch's first write into a shared
 // block gets a private copy.  hyperinfer.ai "KV cache & paged attention deep
 // dive", "What 16-token blocks buy you": evicting a sequence frees its blocks.
+// vaibhawkumar.in "Why LLMs run out of VRAM: KV cache fragmentation and the
+// PagedAttention fix", "PagedAttention: the idea" and "A minimal PyTorch
+// sketch" (truncate): sliding the window releases the oldest whole pages and
+// keeps the rest of the drop as an offset into the first kept page.
+#include <algorithm>
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -182,6 +187,33 @@ pa_status pa_alloc_free_sequence(pa_allocator* a, const int32_t* table_row, int3
         if (a->ref[b] < ++uses[b]) return PA_ERR_INVALID;
     }
     for (int32_t i = 0; i < num_blocks; ++i) pa_alloc_decref(a, table_row[i]);
+    return PA_OK;
+}
+
+pa_status pa_alloc_truncate(pa_allocator* a, int32_t* table_row, int32_t capacity, int32_t* num_blocks,
+                            int32_t* start, int32_t* length, int32_t keep, int32_t block_size) {
+    if (a == nullptr || table_row == nullptr || num_blocks == nullptr || start == nullptr || length == nullptr ||
+        block_size <= 0)
+        return PA_ERR_INVALID;
+    const int32_t nb = *num_blocks, st = *start, len = *length;
+    if (keep < 0 || nb < 0 || nb > capacity || st < 0 || st > len ||
+        static_cast<int64_t>(len) > static_cast<int64_t>(nb) * block_size)
+        return PA_ERR_RANGE;
+    // the new first position; every block wholly before it goes back to the pool
+    const int32_t new_start = std::max(st, len - std::min(keep, len));
+    const int32_t drop = new_start / block_size;
+    std::unordered_map<int32_t, int32_t> uses;
+    for (int32_t i = 0; i < drop; ++i) {
+        const int32_t b = table_row[i];
+        if (!valid_id(a, b)) return PA_ERR_RANGE;
+        if (a->ref[b] < ++uses[b]) return PA_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < drop; ++i) pa_alloc_decref(a, table_row[i]);
+    for (int32_t i = 0; i + drop < nb; ++i) table_row[i] = table_row[i + drop];
+    for (int32_t i = nb - drop; i < nb; ++i) table_row[i] = -1;
+    *num_blocks = nb - drop;
+    *start = new_start - drop * block_size;
+    *length = len - drop * block_size;
     return PA_OK;
 }
 

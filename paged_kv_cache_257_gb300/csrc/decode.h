@@ -16,6 +16,7 @@ struct DecodeArgs {
     const void* v_cache;
     const int32_t* block_tables;  // [batch][max_blocks]
     const int32_t* context_lens;  // [batch]
+    const int32_t* context_starts;  // [batch] first attended position, or null (all 0)
     void* out;                    // [batch][num_q_heads][head_dim] of out_dtype
     float* part_o;                // [batch][num_q_heads][max_parts][head_dim] (split only)
     float* part_ml;               // [batch][num_q_heads][max_parts][2]: (max, sum) in log2 units

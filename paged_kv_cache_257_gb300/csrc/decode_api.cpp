@@ -146,12 +146,13 @@ extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t b
     return layout(cache, batch, num_q_heads, (cap + p - 1) / p).total();
 }
 
-extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
-                                         int32_t num_q_heads, const void* k_cache, const void* v_cache,
-                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                         const int32_t* context_lens, int32_t batch, float scale,
-                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
-                                         void* out, pa_dtype out_dtype, int32_t* device_status, void* stream_) {
+extern "C" pa_status pa_decode_attention_window(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                                int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                const int32_t* context_lens, const int32_t* context_starts,
+                                                int32_t batch, float scale, int32_t partition_size, void* workspace,
+                                                size_t workspace_bytes, void* out, pa_dtype out_dtype,
+                                                int32_t* device_status, void* stream_) {
     pa_status st = check_cache_desc(cache);
     if (st != PA_OK) return st;
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID;
@@ -162,8 +163,8 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     if (batch == 0) return PA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(device_status, 4) ||
-        !aligned(workspace, 16))
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(context_starts, 4) ||
+        !aligned(device_status, 4) || !aligned(workspace, 16))
         return PA_ERR_INVALID;
     const int32_t group = num_q_heads / cache->num_kv_heads;
     const int64_t n_hg = (group + kHeadsPerCta - 1) / kHeadsPerCta;
@@ -184,6 +185,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     a.v_cache = v_cache;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
+    a.context_starts = context_starts;
     a.out = out;
     const WorkspaceLayout wl = layout(cache, batch, num_q_heads, parts);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -212,8 +214,20 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
     a.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
-    a.persistent = (PA_DECODE_PERSISTENT && batch <= kMaxPersistentBatch) ? 1 : 0;
+    // the persistent kernel maps work items without window starts
+    a.persistent = (PA_DECODE_PERSISTENT && batch <= kMaxPersistentBatch && context_starts == nullptr) ? 1 : 0;
     st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
     if (st == PA_OK && parts > 1 && !a.fused_merge) st = launch_decode_reduce(a, s);
     return st;
+}
+
+extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
+                                         int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* context_lens, int32_t batch, float scale,
+                                         int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                         void* out, pa_dtype out_dtype, int32_t* device_status, void* stream) {
+    return pa_decode_attention_window(cache, q, q_dtype, num_q_heads, k_cache, v_cache, block_tables,
+                                      max_blocks_per_seq, context_lens, nullptr, batch, scale, partition_size,
+                                      workspace, workspace_bytes, out, out_dtype, device_status, stream);
 }

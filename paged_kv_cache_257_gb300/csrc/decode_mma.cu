@@ -33,6 +33,7 @@
 #include "common.cuh"
 #include "decode.h"
 #include "decode_epilogue.cuh"
+#include "window.cuh"
 
 namespace pa {
 namespace {
@@ -233,9 +234,11 @@ struct Consumer {
         }
     }
 
-    // One 16-token chunk in stage (kb: K tile, vb: V tile); `valid` tokens of
-    // it are in the context (1..16); `sc` = softmax scale x log2(e) (x K scale).
-    __device__ __forceinline__ void chunk(uint32_t kb, uint32_t vb, int valid, float sc) {
+    // One 16-token chunk in stage (kb: K tile, vb: V tile); its tokens lo..hi-1
+    // are attended (0 <= lo < hi <= 16: lo > 0 only for the chunk holding a slid
+    // window's start, hi < 16 only at the context's end); `sc` = softmax scale
+    // x log2(e) (x K scale).
+    __device__ __forceinline__ void chunk(uint32_t kb, uint32_t vb, int lo, int hi, float sc) {
         // ---- S^T[16 tokens][8 heads] = K Q^T, as two independent accumulation chains
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (!kFp8) {
@@ -264,9 +267,10 @@ struct Consumer {
         // ---- online softmax over this chunk (log2 domain)
         float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
         float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
-        if (valid < kChunk) {
-            if (g >= valid) x0 = x1 = kNegInf;
-            if (g + 8 >= valid) x2 = x3 = kNegInf;
+        const bool partial = lo > 0 || hi < kChunk;
+        if (partial) {
+            if (g < lo || g >= hi) x0 = x1 = kNegInf;
+            if (g + 8 < lo || g + 8 >= hi) x2 = x3 = kNegInf;
         }
         float cm0 = fmaxf(x0, x2), cm1 = fmaxf(x1, x3);
 #pragma unroll
@@ -298,11 +302,12 @@ struct Consumer {
         const uint32_t pb0 = movmatrix_t(pack2<kBf16>(p0, p1));   // tokens 0..7
         const uint32_t pb1 = movmatrix_t(pack2<kBf16>(p2, p3));   // tokens 8..15
 
-        // ---- O^T[128 d][8 heads] += V^T P^T; in the last chunk the rows past
-        // the context hold stale stage data, so their V is zeroed first
-        if (valid < kChunk) {
-            const uint32_t vm01 = (2 * q4 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 1 < valid ? 0xffff0000u : 0u);
-            const uint32_t vm23 = (2 * q4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * q4 + 9 < valid ? 0xffff0000u : 0u);
+        // ---- O^T[128 d][8 heads] += V^T P^T; rows outside lo..hi-1 hold stale
+        // stage data (or another block's), so their V is zeroed first
+        if (partial) {
+            auto in = [&](int t) { return t >= lo && t < hi; };
+            const uint32_t vm01 = (in(2 * q4) ? 0x0000ffffu : 0u) | (in(2 * q4 + 1) ? 0xffff0000u : 0u);
+            const uint32_t vm23 = (in(2 * q4 + 8) ? 0x0000ffffu : 0u) | (in(2 * q4 + 9) ? 0xffff0000u : 0u);
             pv_chunk<KV, C, true>(o, vb, v_row, v_sel, sw, pb0, pb1, vm01, vm23);
         } else {
             pv_chunk<KV, C, false>(o, vb, v_row, v_sel, sw, pb0, pb1, 0u, 0u);
@@ -475,11 +480,12 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
-    const int ctx = clamp_ctx(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
-    const int n_parts = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 1;
+    const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
-    const int tok0 = part * a.partition_size;
-    const int tok1 = min(ctx, tok0 + a.partition_size);
+    const int tok0 = sw.tok0(part, a.partition_size);
+    const int tok1 = sw.tok1(part, a.partition_size);
+    const int lead = sw.lead(part);   // positions of chunk 0 before the window
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
     const int h0 = kvh * a.group + hg * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
@@ -513,6 +519,9 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             const int t0 = tok0 + c * kChunk;
             int pb_a, pb_b;
             win.get(t0, BS, lane, pb_a, pb_b);
+            // an 8-token block wholly before a slid window may have been
+            // released: its rows (masked anyway) come from the chunk's second block
+            if (BS < kChunk && c == 0 && lead >= BS) pb_a = pb_b;
             if (!issue_chunk<C, BS, NSTAGES>(a, &tmap_k, &tmap_v, full, empty, ring, c, lane, kvh, t0, tok1, pb_a,
                                              pb_b, policy)) {
                 if (lane == 0) {
@@ -540,7 +549,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                 break;
             }
             const uint32_t kb = ring + st * C::kStageBytes;
-            cs.chunk(kb, kb + C::kTileBytes, tok1 - (tok0 + c * kChunk), sc);
+            cs.chunk(kb, kb + C::kTileBytes, c == 0 ? lead : 0, min(kChunk, tok1 - (tok0 + c * kChunk)), sc);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(empty + st));
         }
@@ -861,7 +870,7 @@ decode_mma_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const _
                     break;
                 }
                 const uint32_t kb = ring + st * C::kStageBytes;
-                cs.chunk(kb, kb + C::kTileBytes, it.tok1 - (it.tok0 + (k - it.chunk0) * kChunk), sc);
+                cs.chunk(kb, kb + C::kTileBytes, 0, min(kChunk, it.tok1 - (it.tok0 + (k - it.chunk0) * kChunk)), sc);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_addr(empty + st));
             }

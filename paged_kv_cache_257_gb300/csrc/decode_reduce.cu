@@ -12,6 +12,7 @@
 // paged attention deep dive", "Why this matters for long context").
 #include "common.cuh"
 #include "decode.h"
+#include "window.cuh"
 
 namespace pa {
 namespace {
@@ -57,10 +58,7 @@ __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArg
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();      // the partials come from the previous kernel in the stream
     pdl_trigger();
-    int ctx = __ldg(a.context_lens + seq);
-    const int cap = a.max_blocks * a.block_size;
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int n_parts = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 1;
+    const int n_parts = seq_window(a, seq, false).n_parts;
     if (n_parts <= 1) return;
     const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + hq;
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml + row * a.max_parts * 2);

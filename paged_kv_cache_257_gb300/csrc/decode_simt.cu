@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "decode.h"
 #include "decode_epilogue.cuh"
+#include "window.cuh"
 
 namespace pa {
 namespace {
@@ -48,16 +49,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
 
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
-    int ctx = __ldg(a.context_lens + seq);
-    const int cap = a.max_blocks * bs;
-    if (ctx < 0 || ctx > cap) {
-        if (part == 0 && blockIdx.y == 0 && threadIdx.x == 0) raise_flag(a.status, PA_DEVFLAG_CONTEXT_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    const int n_parts = ctx > 0 ? (ctx + a.partition_size - 1) / a.partition_size : 1;
+    const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+    const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
-    const int tok0 = part * a.partition_size;
-    const int tok1 = min(ctx, tok0 + a.partition_size);
+    const int tok0 = sw.tok0(part, a.partition_size);
+    const int tok1 = sw.tok1(part, a.partition_size);
     const int h0 = kvh * a.group + hg * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
     const float sc = a.scale * 1.4426950408889634f;
@@ -83,7 +79,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
     const int32_t* bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
     for (int c0 = tok0 + warp * kChunk; c0 < tok1; c0 += kWarps * kChunk) {
         const int c1 = min(tok1, c0 + kChunk);
-        for (int t = c0; t < c1; ++t) {
+        for (int t = max(c0, sw.start); t < c1; ++t) {
             const int pb = __ldg(bt + t / bs);
             if (pb < 0 || pb >= a.num_blocks) {
                 if (lane == 0) raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);

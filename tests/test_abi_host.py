@@ -256,3 +256,44 @@ def test_plan_partition_rejects_bad_arguments(pa):
         pa.plan_partition(d, 4, 30, 256, [1] * 4, 152)       # 30 query heads over 8 KV heads
     # partition_size's automatic choice is the plan for full sequences on this device
     assert pa.partition_size(d, 4, 32, 256, 0) == pa.plan_partition(d, 4, 32, 256, None, 0)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_allocator_truncate_trace_is_bit_exact(pa, bs):
+    """Appends at each sequence's end, window slides (some with bad
+    arguments), forks and frees: the library and the model agree on every
+    result, row and state dump."""
+    rng = np.random.default_rng(40 + bs)
+    a, m = pa.BlockAllocator(80, 3), OAlloc(80, 3)
+    seqs = []   # [row_a, row_m, nblk, start, length]
+    for step in range(3000):
+        op = rng.integers(0, 8)
+        if op == 0 or not seqs:
+            seqs.append([[-1] * 12, [-1] * 12, 0, 0, 0])
+            continue
+        i = int(rng.integers(len(seqs)))
+        sq = seqs[i]
+        if op in (1, 2, 3):                               # append the next token
+            ra = _apply(a, "append_slot", sq[0], sq[2], sq[4], bs)
+            rm = _apply(m, "append_slot", sq[1], sq[2], sq[4], bs)
+            assert ra == rm and sq[0] == sq[1]
+            if ra[0] == "ok":
+                sq[2], sq[4] = ra[1][1], sq[4] + 1
+        elif op == 4:                                     # slide the window
+            keep = int(rng.integers(-1, 3 * bs))
+            start = sq[3] if rng.integers(0, 10) else sq[4] + 1      # now and then an inconsistent start
+            ra = _apply(a, "truncate", sq[0], sq[2], start, sq[4], keep, bs)
+            rm = _apply(m, "truncate", sq[1], sq[2], start, sq[4], keep, bs)
+            assert ra == rm and sq[0] == sq[1]
+            if ra[0] == "ok":
+                sq[2], sq[3], sq[4] = ra[1]
+        elif op == 5:                                     # fork
+            ra = _apply(a, "fork", sq[0], sq[2])
+            assert ra == _apply(m, "fork", sq[1], sq[2])
+            if ra[0] == "ok":
+                seqs.append([list(sq[0]), list(sq[1]), sq[2], sq[3], sq[4]])
+        else:                                             # finish
+            ra = _apply(a, "free_sequence", sq[0], sq[2])
+            assert ra == _apply(m, "free_sequence", sq[1], sq[2])
+            seqs.pop(i)
+        _same(a, m)
