@@ -357,6 +357,55 @@ pa_status pa_alloc_free_sequence(pa_allocator* a, const int32_t* table_row, int3
 pa_status pa_alloc_dump(const pa_allocator* a, int32_t* free_stack_out, int32_t* free_count_out,
                         int32_t* refcounts_out);
 
+/* ------------------------------------------------ prefix cache (host) */
+
+/* Automatic prefix caching ([DEV] section 5, 2 "Automatic Prefix Caching":
+ * a request whose tokens match a previously computed sequence gets the
+ * matching physical blocks from a hash table mapped into its block table,
+ * skipping their prefill; [HI] "Prefix caching: share the system prompt").
+ * The pages name no hash or policy; the readings taken:
+ *   - only full blocks are cached;
+ *   - block j of a token sequence is keyed by FNV-1a-64 over the
+ *     little-endian bytes of block j-1's key (0 for block 0) followed by
+ *     block j's token ids as 32-bit values (pa_prefix_block_key), so a key
+ *     stands for the whole prefix up to its block;
+ *   - a hit is verified against the stored parent key and token ids, so a
+ *     hash collision never maps a wrong block;
+ *   - the cache holds one reference on every cached block;
+ *   - eviction releases blocks that only the cache still references, least
+ *     recently used first (one match or insert is one use), deeper blocks
+ *     first within a use, then by key.
+ * Not thread-safe: the caller serialises calls on a cache and its allocator.
+ * The allocator must outlive the cache. */
+typedef struct pa_prefix_cache pa_prefix_cache;
+
+/* A cache over `alloc` for blocks of `block_size` tokens. */
+pa_status pa_prefix_create(pa_allocator* alloc, int32_t block_size, pa_prefix_cache** out);
+/* Release the cache's references (in insertion order) and free it. */
+void pa_prefix_destroy(pa_prefix_cache* c);
+/* Key of a block of `num_tokens` token ids whose previous block has key
+ * `parent_key` (0 for the first block).  0 for invalid input. */
+uint64_t pa_prefix_block_key(uint64_t parent_key, const int32_t* tokens, int32_t num_tokens);
+/* Cached blocks, -1 for a null cache. */
+int32_t pa_prefix_size(const pa_prefix_cache* c);
+/* Map the longest cached full-block prefix of a request's token ids (host
+ * [num_tokens]) into table_row[0 .. *matched_blocks) (host, `capacity`
+ * entries); each mapped block gains a reference for the request.  The
+ * request's prefill can skip *matched_blocks * block_size tokens. */
+pa_status pa_prefix_match(pa_prefix_cache* c, const int32_t* tokens, int32_t num_tokens, int32_t* table_row,
+                          int32_t capacity, int32_t* matched_blocks);
+/* Cache the full blocks of a computed sequence: tokens (host [num_tokens])
+ * whose KV sits in table_row[0 .. num_blocks).  Blocks already cached under
+ * their key are only marked used; insertion stops at a key held by other
+ * contents or at a block cached under another key.  *inserted = new
+ * entries.  PA_ERR_RANGE / PA_ERR_INVALID for an id out of range / free, with
+ * nothing changed. */
+pa_status pa_prefix_insert(pa_prefix_cache* c, const int32_t* tokens, int32_t num_tokens, const int32_t* table_row,
+                           int32_t num_blocks, int32_t* inserted);
+/* Release up to `max_blocks` cached blocks that only the cache references
+ * (they return to the allocator's pool); *evicted = how many. */
+pa_status pa_prefix_evict(pa_prefix_cache* c, int32_t max_blocks, int32_t* evicted);
+
 #ifdef __cplusplus
 }
 #endif

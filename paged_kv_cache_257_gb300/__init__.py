@@ -5,10 +5,10 @@ a C ABI, declared in ``include/pagedattn.h``); this package is its Python
 binding.  Build the library with ``paged_kv_cache_257_gb300.build.build()``.
 """
 
-from .api import (AllocError, BlockAllocator, CacheDesc, NativeError, compute_slot_mapping, copy_blocks,
+from .api import (AllocError, BlockAllocator, CacheDesc, NativeError, PrefixCache, compute_slot_mapping, copy_blocks,
                   decode_attention, decode_attention_noalloc, decode_workspace_size, dtype_size, kv_append, kv_bytes_per_token, new_status,
                   new_workspace, partition_size, plan_partition, read_device_status, version)
 
-__all__ = ["AllocError", "BlockAllocator", "CacheDesc", "NativeError", "compute_slot_mapping", "copy_blocks",
+__all__ = ["AllocError", "BlockAllocator", "CacheDesc", "NativeError", "PrefixCache", "compute_slot_mapping", "copy_blocks",
            "decode_attention", "decode_attention_noalloc", "decode_workspace_size", "dtype_size", "kv_append", "kv_bytes_per_token",
            "new_status", "new_workspace", "partition_size", "plan_partition", "read_device_status", "version"]

@@ -71,6 +71,13 @@ SIGNATURES = {
                                             P_int32, P_int32]),
     "pa_alloc_fork": (ctypes.c_int, [c_void_p, c_void_p, c_int32]),
     "pa_alloc_free_sequence": (ctypes.c_int, [c_void_p, c_void_p, c_int32]),
+    "pa_prefix_create": (ctypes.c_int, [c_void_p, c_int32, c_void_p]),
+    "pa_prefix_destroy": (None, [c_void_p]),
+    "pa_prefix_block_key": (c_uint64, [c_uint64, c_void_p, c_int32]),
+    "pa_prefix_size": (c_int32, [c_void_p]),
+    "pa_prefix_match": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_void_p, c_int32, P_int32]),
+    "pa_prefix_insert": (ctypes.c_int, [c_void_p, c_void_p, c_int32, c_void_p, c_int32, P_int32]),
+    "pa_prefix_evict": (ctypes.c_int, [c_void_p, c_int32, P_int32]),
     "pa_alloc_truncate": (ctypes.c_int, [c_void_p, c_void_p, c_int32, P_int32, P_int32, P_int32, c_int32, c_int32]),
     "pa_alloc_dump": (ctypes.c_int, [c_void_p, c_void_p, P_int32, c_void_p]),
 }

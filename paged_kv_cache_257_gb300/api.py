@@ -345,4 +345,56 @@ class BlockAllocator:
 
 __all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
            "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size", "plan_partition",
+           "PrefixCache",
            "decode_workspace_size", "decode_attention", "decode_attention_noalloc", "new_status", "new_workspace", "read_device_status"]
+
+
+class PrefixCache:
+    """The library's prefix cache (``pa_prefix_*``) over a ``BlockAllocator``;
+    same methods as the oracle's model.  Holds its allocator alive."""
+
+    def __init__(self, allocator, block_size):
+        h = ctypes.c_void_p()
+        _alloc_check("pa_prefix_create", lib().pa_prefix_create(allocator._h, block_size, ctypes.byref(h)))
+        self._h, self._alloc, self.bs = h, allocator, block_size
+
+    def __del__(self):
+        self.destroy()
+
+    def destroy(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib().pa_prefix_destroy(h)
+        self._h = None
+
+    @staticmethod
+    def block_key(parent_key, tokens):
+        arr = np.ascontiguousarray(tokens, dtype=np.int32)
+        return int(lib().pa_prefix_block_key(parent_key, arr.ctypes.data, arr.size))
+
+    @property
+    def size(self):
+        return int(lib().pa_prefix_size(self._h))
+
+    def match(self, tokens, table_row):
+        """Maps the cached prefix into ``table_row`` (a list, updated in place); returns the blocks matched."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        arr = (ctypes.c_int32 * len(table_row))(*table_row)
+        m = ctypes.c_int32()
+        _alloc_check("pa_prefix_match", lib().pa_prefix_match(self._h, toks.ctypes.data, toks.size, arr,
+                                                               len(table_row), ctypes.byref(m)))
+        table_row[:] = list(arr)
+        return m.value
+
+    def insert(self, tokens, table_row, num_blocks):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        row = np.ascontiguousarray(table_row[:num_blocks], dtype=np.int32)
+        made = ctypes.c_int32()
+        _alloc_check("pa_prefix_insert", lib().pa_prefix_insert(self._h, toks.ctypes.data, toks.size,
+                                                                 row.ctypes.data, num_blocks, ctypes.byref(made)))
+        return made.value
+
+    def evict(self, max_blocks):
+        n = ctypes.c_int32()
+        _alloc_check("pa_prefix_evict", lib().pa_prefix_evict(self._h, max_blocks, ctypes.byref(n)))
+        return n.value

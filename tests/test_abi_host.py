@@ -297,3 +297,68 @@ def test_allocator_truncate_trace_is_bit_exact(pa, bs):
             assert ra == _apply(m, "free_sequence", sq[1], sq[2])
             seqs.pop(i)
         _same(a, m)
+
+
+def test_prefix_block_key_matches_the_oracle(pa):
+    from oracle import prefix_cache as opc
+    rng = np.random.default_rng(8)
+    for n in (0, 1, 8, 16, 32):
+        toks = rng.integers(-2**31, 2**31 - 1, n, dtype=np.int64).astype(np.int32)
+        parent = int(rng.integers(0, 2**63)) * 2 + 1
+        assert pa.PrefixCache.block_key(parent, toks) == opc.block_key(parent, [int(t) for t in toks])
+
+
+@pytest.mark.parametrize("bs", [8, 16])
+def test_prefix_cache_trace_is_bit_exact(pa, bs):
+    """Requests drawn from a few shared prompts: match, prefill the rest,
+    insert, finish or keep; evictions when the pool runs low.  The library
+    and the model agree on every result, row, cache size and allocator dump."""
+    from oracle import prefix_cache as opc
+    rng = np.random.default_rng(60 + bs)
+    nb = 96
+    la, lm = pa.BlockAllocator(nb, 4), OAlloc(nb, 4)
+    ca, cm = pa.PrefixCache(la, bs), opc.PrefixCache(lm, bs)
+    prompts = [list(map(int, rng.integers(0, 30, 80))) for _ in range(3)]
+    live = []   # (row_a, row_m, nblk)
+    for step in range(600):
+        op = rng.integers(0, 10)
+        if op < 5:                                          # a new request
+            p = prompts[rng.integers(0, 3)]
+            toks = p[:int(rng.integers(0, 81))] + list(map(int, rng.integers(0, 30, int(rng.integers(0, 40)))))
+            ra, rm = [-1] * 16, [-1] * 16
+            ma, mm = ca.match(toks, ra), cm.match(toks, rm)
+            assert ma == mm and ra == rm
+            n, ok = ma, True
+            for t in range(ma * bs, min(len(toks), 16 * bs)):
+                xa = _apply(la, "append_slot", ra, n, t, bs)
+                xm = _apply(lm, "append_slot", rm, n, t, bs)
+                assert xa == xm and ra == rm
+                if xa[0] != "ok":
+                    ok = False
+                    break
+                n = xa[1][1]
+            if ok:
+                ia = _apply(ca, "insert", toks, ra, n)
+                assert ia == _apply(cm, "insert", toks, rm, n)
+            live.append((ra, rm, n))
+        elif op < 8 and live:                               # a request finishes
+            ra, rm, n = live.pop(int(rng.integers(len(live))))
+            assert _apply(la, "free_sequence", ra, n) == _apply(lm, "free_sequence", rm, n)
+        else:                                               # make room
+            k = int(rng.integers(0, 12))
+            assert ca.evict(k) == cm.evict(k)
+        assert ca.size == cm.size
+        _same(la, lm)
+    ca.destroy(), cm.destroy()
+    _same(la, lm)
+
+
+def test_prefix_cache_insert_errors(pa):
+    al = pa.BlockAllocator(8)
+    c = pa.PrefixCache(al, 4)
+    with pytest.raises(pa.AllocError) as e:
+        c.insert(list(range(8)), [0, 1], 2)        # free blocks
+    assert e.value.status == "INVALID" and c.size == 0 and al.free_count == 8
+    with pytest.raises(pa.AllocError) as e:
+        c.insert(list(range(4)), [99], 1)
+    assert e.value.status == "RANGE"
