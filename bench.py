@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--workload", default="gqa_bf16")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--partition", type=int, default=None, help="tokens per partition (default: the workload's)")
+    p.add_argument("--window", type=int, default=0,
+                   help="attend only each sequence's last W tokens (a slid window; 0: the whole context)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle baseline sample")
     p.add_argument("--clock-probe-s", type=float, default=2.0,
@@ -127,7 +129,7 @@ class ClockSampler:
 class GpuWorkload:
     """A workload's caches, block tables and step inputs on the device."""
 
-    def __init__(self, name, device, replicas, partition=None):
+    def __init__(self, name, device, replicas, partition=None, window=0):
         import torch
 
         import paged_kv_cache_257_gb300 as pa
@@ -142,6 +144,9 @@ class GpuWorkload:
         # 0 = the library plans it from the batch's context lengths, which a
         # serving host knows when it builds the block tables
         self.plan = self.partition == 0
+        # a slid window: positions [ctx - W, ctx) of each row are attended
+        self.window = window
+        self.starts_host = np.maximum(ctx - window, 0).astype(np.int32) if window > 0 else None
         # source values of every cached token (in the cache's source type)
         k_scale = v_scale = 1.0
         seqs_k, seqs_v = [], []
@@ -179,10 +184,10 @@ class GpuWorkload:
                 pa.kv_append(self.desc, k, v, sl, kc, vc)
         del allk, allv
         torch.cuda.synchronize()
-        self.kv_tokens = int(np.sum(ctx))
+        self.kv_tokens = int(np.sum(ctx - (self.starts_host if window > 0 else 0)))
         self.kv_bytes = self.kv_tokens * 2 * w.n_kv_heads * w.head_dim * w.kv_elem_bytes
         self.unique_kv_bytes = self.kv_bytes
-        if w.prefix_len:
+        if w.prefix_len and window <= 0:
             uniq = w.prefix_len + int(np.sum(ctx - w.prefix_len))
             self.unique_kv_bytes = uniq * 2 * w.n_kv_heads * w.head_dim * w.kv_elem_bytes
         # step inputs
@@ -194,6 +199,9 @@ class GpuWorkload:
         self.block_tables = torch.from_numpy(self.tables_np).to(device)
         self.context_lens = torch.from_numpy(ctx.astype(np.int32)).to(device)
         self.ctx_host = ctx.astype(np.int32)
+        self.context_starts = None
+        if window > 0:
+            self.context_starts = torch.from_numpy(self.starts_host).to(device)
         if self.plan:
             self.partition = self.plan_partition()
         self.new_k, self.new_v, self.new_slots = self.step_append_inputs(wl, dev)
@@ -220,7 +228,10 @@ class GpuWorkload:
 
     def plan_partition(self):
         w = self.w
-        return self.pa.plan_partition(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], self.ctx_host)
+        lens = self.ctx_host
+        if self.starts_host is not None:        # a window's partitions start at its start rounded down to 16
+            lens = self.ctx_host - (self.starts_host & ~15)
+        return self.pa.plan_partition(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1], lens)
 
     def step_append_inputs(self, wl, dev):
         torch = self.torch
@@ -246,7 +257,8 @@ class GpuWorkload:
         if decode_events is not None:
             decode_events[0].record()
         pa.decode_attention(self.desc, self.q, kc, vc, self.block_tables, self.context_lens, self.w.scale,
-                            partition=self.partition, workspace=self.workspace, out=self.out)
+                            partition=self.partition, workspace=self.workspace, out=self.out,
+                            context_starts=self.context_starts)
         if decode_events is not None:
             decode_events[1].record()
         return n + 1 + (1 if self.workspace is not None else 0)
@@ -271,6 +283,43 @@ def captured_traffic(workload):
         with open(os.path.join(root, f), "rb") as fh:
             h.update(fh.read())
     return NCU_TRAFFIC.get(h.hexdigest()[:16], {}).get(workload)
+
+
+def prefix_cache_host_timing(pa, w):
+    """Host cost of the prefix cache on this workload's shape: one request
+    computes and caches the shared prefix; each of the others maps it
+    (pa_prefix_match) and caches its own full blocks (pa_prefix_insert).
+    Token ids are seeded synthetic values."""
+    import synth
+    bs = w.block_size
+    alloc = pa.BlockAllocator(w.num_blocks, 1)
+    cache = pa.PrefixCache(alloc, bs)
+    prefix = [int(x) for x in synth.uniform_int(90, 0, w.prefix_len, 0, 1 << 17)]
+    cap = -(-int(max(w.context_lens) + 1) // bs)
+    rows, match_s, insert_s, matched = [], 0.0, 0.0, 0
+    for s in range(w.batch):
+        n_tok = int(w.context_lens[s]) + 1
+        toks = prefix + [int(x) for x in synth.uniform_int(91, s, n_tok - w.prefix_len, 0, 1 << 17)]
+        row = [-1] * cap
+        t0 = time.perf_counter()
+        m = cache.match(toks, row)
+        match_s += time.perf_counter() - t0
+        matched += m
+        n = m
+        for t in range(m * bs, n_tok):
+            _, n, _ = alloc.append_slot(row, n, t, bs)
+        t0 = time.perf_counter()
+        cache.insert(toks, row, n)
+        insert_s += time.perf_counter() - t0
+        rows.append((row, n))
+    blocks_private = sum(-(-(int(c) + 1) // bs) for c in w.context_lens)
+    out = {"requests": w.batch, "prefix_tokens": w.prefix_len,
+           "match_us_per_request": match_s / w.batch * 1e6, "insert_us_per_request": insert_s / w.batch * 1e6,
+           "blocks_matched": matched, "blocks_held": w.num_blocks - alloc.free_count,
+           "blocks_without_sharing": blocks_private,
+           "note": "host-side, through the Python binding (ctypes); not in the timed GPU region"}
+    cache.destroy()
+    return out
 
 
 def time_device(wk, steps, warmup, probe_s=0.0):
@@ -309,6 +358,8 @@ def time_e2e(wk, steps, warmup):
     torch, pa = wk.torch, wk.pa
     host = {"q": wk.q.cpu().pin_memory(), "bt": wk.block_tables.cpu().pin_memory(),
             "ctx": wk.context_lens.cpu().pin_memory()}
+    if wk.context_starts is not None:
+        host["starts"] = wk.context_starts.cpu().pin_memory()
     if wk.new_k is not None:
         host.update(k=wk.new_k.cpu().pin_memory(), v=wk.new_v.cpu().pin_memory(),
                     slots=wk.new_slots.cpu().pin_memory())
@@ -325,7 +376,7 @@ def time_e2e(wk, steps, warmup):
             pa.kv_append(wk.desc, dev["k"], dev["v"], dev["slots"], kc, vc)
         part = wk.plan_partition() if wk.plan else wk.partition   # host work of a serving step
         pa.decode_attention(wk.desc, dev["q"], kc, vc, dev["bt"], dev["ctx"], wk.w.scale,
-                            partition=part, workspace=wk.workspace, out=wk.out)
+                            partition=part, workspace=wk.workspace, out=wk.out, context_starts=dev.get("starts"))
         out_host.copy_(wk.out, non_blocking=True)
 
     for i in range(warmup):
@@ -381,22 +432,25 @@ def oracle_setup(w_name):
     return _ORACLE_SETUP[w_name]
 
 
-def oracle_step_sample(w_name, budget_s):
+def oracle_step_sample(w_name, budget_s, window=0):
     """Time the oracle's paged decode attention on the host for about ``budget_s``.
 
     Returns (decode tokens per second, sequence-steps run, seconds, sample text)."""
     from oracle import attention as oatt  # test infrastructure: the CPU baseline leg only
     w, seqs, q, kp, vp, tables, ctx, (ks, vs) = oracle_setup(w_name)
+    starts = np.maximum(ctx - window, 0) if window > 0 else None
     t0 = time.perf_counter()
     done = 0
     while True:
-        oatt.decode_attention_paged(q, kp, vp, tables, ctx, w.scale, w.kv_dtype, ks, vs, q_dtype=w.q_dtype)
+        oatt.decode_attention_paged(q, kp, vp, tables, ctx, w.scale, w.kv_dtype, ks, vs, q_dtype=w.q_dtype,
+                                    context_starts=starts)
         done += len(seqs)
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     sample = (f"oracle decode_attention_paged (numpy, float64) over {len(seqs)} of {w.batch} sequences of "
-              f"{w_name} (their block tables and context lengths), {done} sequence-steps in {dt:.1f} s")
+              f"{w_name} (their block tables and context lengths"
+              + (f", last {window} tokens" if window > 0 else "") + f"), {done} sequence-steps in {dt:.1f} s")
     return done / dt, done, dt, sample
 
 
@@ -450,7 +504,7 @@ def main():
     # enough replicas of the caches that their total exceeds L2 several times
     per = w.num_blocks * w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes * 2
     replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
-    wk = GpuWorkload(args.workload, device, replicas, args.partition)
+    wk = GpuWorkload(args.workload, device, replicas, args.partition, args.window)
     with ClockSampler(local) as clk:
         total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
     e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
@@ -471,7 +525,8 @@ def main():
                    "kv_dtype": w.kv_dtype, "q_dtype": w.q_dtype, "kv_tokens": wk.kv_tokens,
                    "partition_size": wk.resolved_partition, "append_tokens": w.append_tokens,
                    "l2": f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"window": args.window} if args.window > 0 else {})},
         "kv_tokens_per_s": wk.kv_tokens * world / step_s,
         "kv_gbs": wk.kv_bytes * world / step_s / 1e9,
         "decode_kernel_us": dec_avg_s * 1e6,
@@ -485,8 +540,10 @@ def main():
     }
     if wk.unique_kv_bytes != wk.kv_bytes:
         line["unique_kv_gbs"] = wk.unique_kv_bytes * world / step_s / 1e9
+    if w.prefix_len and rank == 0:
+        line["prefix_cache"] = prefix_cache_host_timing(wk.pa, w)
     if rank == 0 and not args.no_cpu_baseline:
-        v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds)
+        v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds, args.window)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
@@ -502,12 +559,12 @@ def run_reference(args):
     w = wl.make(args.workload)
     per_step = max(1.0, min(10.0, 60.0 / max(1, args.steps)))
     for _ in range(args.warmup):
-        oracle_step_sample(args.workload, 0.0)
+        oracle_step_sample(args.workload, 0.0, args.window)
     t0 = time.perf_counter()
     total = 0
     sample = ""
     for _ in range(args.steps):
-        _, done, _, sample = oracle_step_sample(args.workload, per_step)
+        _, done, _, sample = oracle_step_sample(args.workload, per_step, args.window)
         total += done
     dt = time.perf_counter() - t0
     value = total / dt
@@ -516,7 +573,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "batch": w.batch, "n_q_heads": w.n_q_heads,
                        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                       "kv_dtype": w.kv_dtype, "parallelism": "host cores"},
+                       "kv_dtype": w.kv_dtype, "parallelism": "host cores",
+                       **({"window": args.window} if args.window > 0 else {})},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
