@@ -208,8 +208,11 @@ struct Consumer {
     // Q as the B operand of S^T = K Q^T: column n = head g, 16 rows of d per
     // k-step.  `rows` points at the first head's row (nh rows of kD 16-bit
     // elements); GLOBAL selects read-only global loads over generic ones.
+    // load_q = fetch_q (the loads alone, so a caller can overlap them with
+    // other waits) then convert_q (FP8 caches: the query widened to f16 in the
+    // K operand's d order).
     template <bool GLOBAL>
-    __device__ __forceinline__ void load_q(const uint16_t* rows, int nh, bool q_bf16) {
+    __device__ __forceinline__ void fetch_q(const uint16_t* rows, int nh) {
         const bool hv = g < nh;
         const uint16_t* row = rows + (hv ? g : 0) * kD;
 #pragma unroll
@@ -221,17 +224,31 @@ struct Consumer {
                 qf[kk][1] = hv ? (GLOBAL ? __ldg(p1) : *p1) : 0u;
             } else {
                 // FP8 tiles give each thread 4 consecutive codes per row and k-step
-                // (d = 16kk + 4q + 0..3); fp8_q_pairs orders them like fp8_k_pairs
+                // (d = 16kk + 4q + 0..3): the query's d = 16kk + 4q + 0..3 raw
                 const uint2* p = reinterpret_cast<const uint2*>(row + 16 * kk + 4 * q4);
                 const uint2 raw = hv ? (GLOBAL ? __ldg(p) : *p) : make_uint2(0u, 0u);
-                uint32_t h01 = raw.x, h23 = raw.y;
-                if (q_bf16) {   // bf16 -> float (exact) -> f16
-                    h01 = pack2<false>(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u));
-                    h23 = pack2<false>(__uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u));
-                }
-                fp8_q_pairs(h01, h23, qf[kk][0], qf[kk][1]);
+                qf[kk][0] = raw.x;
+                qf[kk][1] = raw.y;
             }
         }
+    }
+    __device__ __forceinline__ void convert_q(bool q_bf16) {
+        if constexpr (kFp8) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t h01 = qf[kk][0], h23 = qf[kk][1];
+                if (q_bf16) {   // bf16 -> float (exact) -> f16
+                    h01 = pack2<false>(__uint_as_float(h01 << 16), __uint_as_float(h01 & 0xffff0000u));
+                    h23 = pack2<false>(__uint_as_float(h23 << 16), __uint_as_float(h23 & 0xffff0000u));
+                }
+                fp8_q_pairs(h01, h23, qf[kk][0], qf[kk][1]);   // ordered like fp8_k_pairs
+            }
+        }
+    }
+    template <bool GLOBAL>
+    __device__ __forceinline__ void load_q(const uint16_t* rows, int nh, bool q_bf16) {
+        fetch_q<GLOBAL>(rows, nh);
+        convert_q(q_bf16);
     }
 
     // One 16-token chunk in stage (kb: K tile, vb: V tile); its tokens lo..hi-1
@@ -478,8 +495,32 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int kvh = blockIdx.y / n_hg, hg = blockIdx.y - kvh * n_hg;
     const int part = blockIdx.x;
 
+    const int h0 = kvh * a.group + hg * kHeadsPerCta;
+    const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
+    const int32_t* bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
+
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
+    // The context length, the partition's first block ids and the query do
+    // not depend on one another: issue all three loads before waiting on
+    // any, so a CTA's first copy waits for one round trip less.  Without
+    // window starts a partition's blocks begin at part * P / block_size.
+    Consumer<KV, C> cs;
+    cs.init(lane);
+    cs.reset();
+    const bool spec = a.context_starts == nullptr;
+    int spec_ids = 0;
+    if (warp == kConsumers) {
+        if (lane == 0) {
+            prefetch_tmap(&tmap_k);
+            prefetch_tmap(&tmap_v);
+        }
+        const int j = part * (a.partition_size / BS) + lane;
+        if (spec && j < a.max_blocks) spec_ids = __ldg(bt_row + j);
+    } else {
+        cs.template fetch_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
+                                  nh);
+    }
     const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
@@ -487,8 +528,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int tok1 = sw.tok1(part, a.partition_size);
     const int lead = sw.lead(part);   // positions of chunk 0 before the window
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
-    const int h0 = kvh * a.group + hg * kHeadsPerCta;
-    const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGES; ++i) {
@@ -500,19 +539,14 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     __syncthreads();
 
-    Consumer<KV, C> cs;
-    cs.init(lane);
-    cs.reset();
-
     if (warp == kConsumers) {
         // ------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
         const uint64_t policy = l2_evict_first_policy();
         BlockWindow win;
-        win.start(a.block_tables + static_cast<int64_t>(seq) * a.max_blocks, tok0, tok1, BS);
+        if (spec)
+            win.start_loaded(bt_row, tok0, tok1, BS, spec_ids);
+        else
+            win.start(bt_row, tok0, tok1, BS);
         int issued = 0;
         for (int c = 0; c < n_chunks; ++c) {
             if (*reinterpret_cast<volatile int*>(abort_flag)) break;
@@ -536,8 +570,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     } else {
         // ------------------------------------------------------ consumers
         const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale * kFp8WidenScale : 1.f);
-        cs.template load_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
-                                 nh, a.q_dtype == PA_BF16);
+        cs.convert_q(a.q_dtype == PA_BF16);
         for (int c = warp; c < n_chunks; c += kConsumers) {
             const int st = c % NSTAGES;
             const bool landed = mbar_wait(smem_addr(full + st), (c / NSTAGES) & 1);
