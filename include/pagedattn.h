@@ -164,11 +164,11 @@ int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int3
                                  int32_t max_blocks_per_seq, int32_t requested);
 
 /* Bytes of device workspace pa_decode_attention needs for these arguments:
- * 256 bytes of work-scheduling counters, plus, when contexts are split, the
- * merge counters and the partial softmax state of the partitions.  Returns 0
- * for invalid input.  The workspace must be zero-filled before its first
- * use; every completed call leaves its counters at zero again, so one
- * zeroed buffer serves any sequence of calls that are not concurrent. */
+ * when contexts are split, the merge counters and the partial softmax state
+ * of the partitions; 0 when every sequence fits one partition (or for
+ * invalid input).  The workspace must be zero-filled before its first use;
+ * every completed call leaves its counters at zero again, so one zeroed
+ * buffer serves any sequence of calls that are not concurrent. */
 /* Partition size for a batch whose context lengths the host knows (a
  * serving loop knows them: it built the block tables).  The pages do not
  * size partitions; this models a call as waves of work items (one per

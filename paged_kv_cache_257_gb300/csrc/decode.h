@@ -20,10 +20,8 @@ struct DecodeArgs {
     void* out;                    // [batch][num_q_heads][head_dim] of out_dtype
     float* part_o;                // [batch][num_q_heads][max_parts][head_dim] (split only)
     float* part_ml;               // [batch][num_q_heads][max_parts][2]: (max, sum) in log2 units
-    int32_t* sched;               // persistent kernel: [0] next item, [1] CTAs done; zero between calls
     int32_t* tickets;             // [batch][num_kv_heads * head groups], zero between calls
     int32_t fused_merge;          // 1: the last CTA of a group merges; 0: the merge kernel does
-    int32_t persistent;           // 1: resident CTAs take items from `sched` (batch <= kMaxPersistentBatch)
     int32_t* status;              // device status word or null
     int32_t batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks;
     int32_t group;                // num_q_heads / num_kv_heads
@@ -46,12 +44,8 @@ constexpr int kHeadsPerCta = 8;
 // Up to this many partitions per sequence the decode kernel merges them itself.
 constexpr int kFusedMergeMaxParts = 16;
 
-// Largest batch the persistent tensor-core kernel maps items for (its prefix
-// sums over the batch live in shared memory); larger batches use one CTA per item.
-constexpr int kMaxPersistentBatch = 1024;
-
 // Bytes at the front of the decode workspace holding counters that must be
-// zero when a call starts (scheduler counters and merge tickets).
+// zero when a call starts (the merge tickets).
 size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                             int32_t partition_size);
 

@@ -12,25 +12,16 @@ namespace {
 
 constexpr int kMaxParts = 32768;
 
-// 1: batches up to kMaxPersistentBatch run the persistent tensor-core kernel;
-// 0: every batch runs one CTA per work item.
-#ifndef PA_DECODE_PERSISTENT
-#define PA_DECODE_PERSISTENT 0
-#endif
-
-// Workspace layout: scheduler counters (256 B), then for a split call the
-// merge tickets, partial outputs and partial (max, sum) pairs.
-constexpr size_t kSchedBytes = 256;
-
+// Workspace layout of a split call: merge tickets, partial outputs and
+// partial (max, sum) pairs.  An unsplit call needs none.
 struct WorkspaceLayout {
-    size_t sched_bytes, tickets_bytes, part_o_bytes, part_ml_bytes;
-    size_t total() const { return sched_bytes + tickets_bytes + part_o_bytes + part_ml_bytes; }
+    size_t tickets_bytes, part_o_bytes, part_ml_bytes;
+    size_t total() const { return tickets_bytes + part_o_bytes + part_ml_bytes; }
 };
 
 WorkspaceLayout layout(const pa_cache_desc* c, int64_t batch, int64_t num_q_heads, int64_t parts) {
     const int64_t groups = (num_q_heads / c->num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
     WorkspaceLayout w{};
-    w.sched_bytes = kSchedBytes;
     if (parts <= 1) return w;
     w.tickets_bytes = (static_cast<size_t>(batch * c->num_kv_heads * groups) * sizeof(int32_t) + 255) / 256 * 256;
     w.part_o_bytes = static_cast<size_t>(batch * num_q_heads * parts * c->head_dim) * sizeof(float);
@@ -133,7 +124,7 @@ size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q
     if (p <= 0) return 0;
     const int64_t cap = static_cast<int64_t>(max_blocks) * c->block_size;
     const WorkspaceLayout w = layout(c, batch, num_q_heads, (cap + p - 1) / p);
-    return w.sched_bytes + w.tickets_bytes;
+    return w.tickets_bytes;
 }
 
 }  // namespace pa
@@ -189,11 +180,10 @@ extern "C" pa_status pa_decode_attention_window(const pa_cache_desc* cache, cons
     a.out = out;
     const WorkspaceLayout wl = layout(cache, batch, num_q_heads, parts);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    a.sched = reinterpret_cast<int32_t*>(ws);
     const bool split = wl.tickets_bytes > 0;
-    a.tickets = split ? reinterpret_cast<int32_t*>(ws + wl.sched_bytes) : nullptr;
-    a.part_o = split ? reinterpret_cast<float*>(ws + wl.sched_bytes + wl.tickets_bytes) : nullptr;
-    a.part_ml = split ? reinterpret_cast<float*>(ws + wl.sched_bytes + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
+    a.tickets = split ? reinterpret_cast<int32_t*>(ws) : nullptr;
+    a.part_o = split ? reinterpret_cast<float*>(ws + wl.tickets_bytes) : nullptr;
+    a.part_ml = split ? reinterpret_cast<float*>(ws + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
     a.fused_merge = parts <= kFusedMergeMaxParts ? 1 : 0;
     a.status = device_status;
     a.batch = batch;
@@ -214,8 +204,6 @@ extern "C" pa_status pa_decode_attention_window(const pa_cache_desc* cache, cons
     a.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
-    // the persistent kernel maps work items without window starts
-    a.persistent = (PA_DECODE_PERSISTENT && batch <= kMaxPersistentBatch && context_starts == nullptr) ? 1 : 0;
     st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
     if (st == PA_OK && parts > 1 && !a.fused_merge) st = launch_decode_reduce(a, s);
     return st;

@@ -20,12 +20,7 @@
 //     operand with two movmatrix transposes and accumulates O^T = V^T P^T;
 //   * the warps' (max, sum, output) states are merged and written as the
 //     final output or, for a split context, as a partition partial.
-// Two kernels share these pieces.  The persistent kernel (batches up to
-// kMaxPersistentBatch) runs one CTA per resident slot; each CTA takes items
-// from an atomic counter -- every full partition first, partial ones after --
-// and its producer streams the next item's tiles while the consumers finish
-// and merge the current one.  The grid kernel runs one CTA per item.
-// FP8 tiles are widened to float16 in registers, with the K scale folded into
+// The grid runs one CTA per item.  FP8 tiles are widened to float16 in registers, with the K scale folded into
 // the score scale and the V scale into the output.
 #include <algorithm>
 #include <mutex>
@@ -438,16 +433,6 @@ __device__ __forceinline__ void drain_ring(const DecodeArgs& a, uint64_t* full, 
     }
 }
 
-__device__ __forceinline__ int clamp_ctx(const DecodeArgs& a, int seq, bool report) {
-    int ctx = __ldg(a.context_lens + seq);
-    const int cap = a.max_blocks * a.block_size;
-    if (ctx < 0 || ctx > cap) {
-        if (report) raise_flag(a.status, PA_DEVFLAG_CONTEXT_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    return ctx;
-}
-
 // Write one merged value: the final output, or this partition's partial.
 __device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, int d, int part, int n_parts,
                                              float val, float M, float L) {
@@ -638,350 +623,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
 }
 
-// =====================================================================
-// Persistent kernel: resident CTAs take items from an atomic counter
-// =====================================================================
-
-constexpr int kQueue = 4;   // item descriptors (and their query rows) in flight per CTA
-
-// Item order: full partitions of every sequence first (sequence, partition,
-// head group), then each sequence's last, partial partition.  The producer
-// maps a counter value to an item through two prefix sums over the batch.
-struct Item {
-    int seq, grp, part, tok0, tok1, chunk0, n_chunks, n_parts;
-};
-
-template <pa_dtype KV, int BS, int NSTAGES>
-struct PersistCfg : Cfg<KV, BS, NSTAGES> {
-    using B = Cfg<KV, BS, NSTAGES>;
-    static constexpr int kQSlotBytes = kHeadsPerCta * kD * 2;                 // one item's query rows
-    static constexpr int kOffQ = B::kRingBytes;
-    static constexpr int kOffAcc = kOffQ + kQueue * kQSlotBytes;              // [8 heads][kMergeStride] f32
-    static constexpr int kOffWarpML = kOffAcc + kHeadsPerCta * kMergeStride * 4;   // [2][4 warps][8] f32
-    static constexpr int kOffPrefix = kOffWarpML + 2 * kConsumers * kHeadsPerCta * 4;  // 2 x (batch + 1) int32
-    static constexpr int kOffDesc = kOffPrefix + 2 * (kMaxPersistentBatch + 1) * 4;
-    static constexpr int kOffBars = (kOffDesc + kQueue * static_cast<int>(sizeof(Item)) + 7) / 8 * 8;
-    static constexpr int kOffFlags = kOffBars + (2 * NSTAGES + 2 * kQueue) * 8;
-    static constexpr int kSmemBytes = 1024 + kOffFlags + 16;
-};
-
-// named barrier of the four consumer warps (the producer never joins it)
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// the same barrier, returning whether `pred` held for any consumer thread:
-// every consumer warp gets the same answer, so branches on it stay uniform
-__device__ __forceinline__ bool consumer_bar_any(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
-
-// largest s in [0, n) with pre[s] <= x (pre non-decreasing, pre[0] == 0)
-__device__ __forceinline__ int prefix_search(const int* pre, int n, int x) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid] <= x) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-template <pa_dtype KV, int BS, int NSTAGES>
-__global__ void __launch_bounds__(kThreads, 4)
-decode_mma_persistent_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                             const DecodeArgs a) {
-    using C = PersistCfg<KV, BS, NSTAGES>;
-    constexpr bool kFp8 = KV == PA_FP8_E4M3;
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring = smem_addr(smem);
-    uint8_t* qslots = smem + C::kOffQ;
-    float* acc = reinterpret_cast<float*>(smem + C::kOffAcc);
-    float* wm = reinterpret_cast<float*>(smem + C::kOffWarpML);      // [warp][head] max
-    float* wl = wm + kConsumers * kHeadsPerCta;                       // [warp][head] sum
-    int* pre_full = reinterpret_cast<int*>(smem + C::kOffPrefix);     // [batch + 1]
-    int* pre_part = pre_full + (kMaxPersistentBatch + 1);             // [batch + 1]
-    Item* desc = reinterpret_cast<Item*>(smem + C::kOffDesc);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* empty = full + NSTAGES;
-    uint64_t* item_full = empty + NSTAGES;
-    uint64_t* item_empty = item_full + kQueue;
-    int* abort_flag = reinterpret_cast<int*>(smem + C::kOffFlags);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
-    const int n_grp = a.num_kv_heads * n_hg;
-    const int P = a.partition_size;
-    int* sched = a.sched;          // [0]: next item, [1]: CTAs done
-
-    pdl_wait();      // inputs may come from the previous kernel in the stream
-    pdl_trigger();
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGES; ++i) {
-            mbar_init(smem_addr(full + i), 1);
-            mbar_init(smem_addr(empty + i), 1);
-        }
-        for (int i = 0; i < kQueue; ++i) {
-            mbar_init(smem_addr(item_full + i), 1);
-            mbar_init(smem_addr(item_empty + i), 1);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    for (int i = threadIdx.x; i < kHeadsPerCta * kMergeStride; i += blockDim.x) acc[i] = 0.f;
-    __syncthreads();
-
-    if (warp == kConsumers) {
-        // ------------------------------------------------------ producer
-        if (lane == 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
-        // prefix sums over the batch: full partitions, and "has a partial one"
-        // (an empty sequence counts as one partial partition: it writes zeros)
-        {
-            const int per = (a.batch + 31) / 32;
-            const int s0 = min(a.batch, lane * per), s1 = min(a.batch, s0 + per);
-            int nf = 0, np = 0;
-            for (int s = s0; s < s1; ++s) {
-                const int c = clamp_ctx(a, s, blockIdx.x == 0);
-                nf += c / P;
-                np += (c % P != 0 || c == 0) ? 1 : 0;
-            }
-            int fi = nf, pi = np;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int fu = __shfl_up_sync(0xffffffffu, fi, off), pu = __shfl_up_sync(0xffffffffu, pi, off);
-                if (lane >= off) { fi += fu; pi += pu; }
-            }
-            int fr = fi - nf, pr = pi - np;
-            for (int s = s0; s < s1; ++s) {
-                const int c = clamp_ctx(a, s, false);
-                pre_full[s] = fr;
-                pre_part[s] = pr;
-                fr += c / P;
-                pr += (c % P != 0 || c == 0) ? 1 : 0;
-            }
-            if (lane == 31) {
-                pre_full[a.batch] = fi;
-                pre_part[a.batch] = pi;
-            }
-            __syncwarp();
-        }
-        const int total_full = pre_full[a.batch];
-        const int total = (total_full + pre_part[a.batch]) * n_grp;
-        const uint64_t policy = l2_evict_first_policy();
-        const int cap = a.max_blocks * BS;
-        // Items are looked ahead: while item n's tiles are issued, the index of
-        // item n+2 is being fetched and item n+1's context length and first 32
-        // block ids are in flight, so no item waits on those round trips.
-        struct Ahead {
-            int idx, s, part, grp, ctx_raw, ids;
-        };
-        auto locate = [&](int idx) {
-            Ahead h{idx, 0, 0, 0, 0, 0};
-            if (idx < total) {
-                int j = idx / n_grp;
-                h.grp = idx - j * n_grp;
-                if (j < total_full) {
-                    h.s = prefix_search(pre_full, a.batch, j);
-                    h.part = j - pre_full[h.s];
-                } else {
-                    j -= total_full;
-                    h.s = prefix_search(pre_part, a.batch, j);
-                    h.part = pre_full[h.s + 1] - pre_full[h.s];
-                }
-                h.ctx_raw = __ldg(a.context_lens + h.s);
-                const int jb = h.part * P / BS + lane;
-                h.ids = jb < a.max_blocks ? __ldg(a.block_tables + static_cast<int64_t>(h.s) * a.max_blocks + jb) : 0;
-            }
-            return h;
-        };
-        int pend = lane == 0 ? atomicAdd(sched, 1) : 0;
-        Ahead cur = locate(__shfl_sync(0xffffffffu, pend, 0));
-        pend = lane == 0 ? atomicAdd(sched, 1) : 0;   // index of the item after `cur`, in flight
-        int k = 0;        // chunks issued (global chunk counter of this CTA)
-        int n = 0;        // items issued
-        bool ok = true;
-        while (ok) {
-            const int slot = n % kQueue;
-            if (n >= kQueue) {
-                int w = 1;
-                if (lane == 0) w = mbar_wait(smem_addr(item_empty + slot), ((n / kQueue) - 1) & 1);
-                if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-            }
-            if (*reinterpret_cast<volatile int*>(abort_flag)) { ok = false; break; }
-            if (cur.idx >= total) {   // no work left: tell the consumers
-                if (lane == 0) {
-                    desc[slot].seq = -1;
-                    mbar_arrive(smem_addr(item_full + slot));
-                }
-                break;
-            }
-            const Ahead nxt = locate(__shfl_sync(0xffffffffu, pend, 0));
-            pend = lane == 0 ? atomicAdd(sched, 1) : 0;
-            const int ctx = cur.ctx_raw < 0 ? 0 : min(cur.ctx_raw, cap);
-            Item it;
-            it.seq = cur.s;
-            it.grp = cur.grp;
-            it.part = cur.part;
-            it.tok0 = cur.part * P;
-            it.tok1 = min(ctx, it.tok0 + P);
-            it.chunk0 = k;
-            it.n_chunks = it.tok1 > it.tok0 ? (it.tok1 - it.tok0 + kChunk - 1) / kChunk : 0;
-            it.n_parts = ctx > 0 ? (ctx + P - 1) / P : 1;
-            const int kvh = cur.grp / n_hg;
-            const int h0 = kvh * a.group + (cur.grp - kvh * n_hg) * kHeadsPerCta;
-            const int nh = min(kHeadsPerCta, a.group - (cur.grp - kvh * n_hg) * kHeadsPerCta);
-            if (lane == 0) {
-                desc[slot] = it;
-                const uint32_t fb = smem_addr(item_full + slot);
-                const uint32_t qbytes = nh * kD * 2;
-                mbar_arrive_expect_tx(fb, qbytes);
-                bulk_load(smem_addr(qslots + slot * C::kQSlotBytes),
-                          static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(cur.s) * a.num_q_heads + h0) * kD,
-                          qbytes, fb);
-            }
-            __syncwarp();
-            BlockWindow win;
-            win.start_loaded(a.block_tables + static_cast<int64_t>(cur.s) * a.max_blocks, it.tok0, it.tok1, BS,
-                             cur.ids);
-            for (int c = 0; c < it.n_chunks; ++c) {
-                const int t0 = it.tok0 + c * kChunk;
-                int pb_a, pb_b;
-                win.get(t0, BS, lane, pb_a, pb_b);
-                if (!issue_chunk<C, BS, NSTAGES>(a, &tmap_k, &tmap_v, full, empty, ring, k, lane, kvh, t0, it.tok1,
-                                                 pb_a, pb_b, policy)) {
-                    ok = false;
-                    break;
-                }
-                ++k;
-            }
-            cur = nxt;
-            ++n;
-        }
-        if (!ok && lane == 0) {
-            atomicExch(abort_flag, 1);
-            raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-        }
-        drain_ring<NSTAGES>(a, full, k, lane);
-    } else {
-        // ------------------------------------------------------ consumers
-        const int tid = threadIdx.x;   // 0..127
-        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale * kFp8WidenScale : 1.f);
-        const float vs = kFp8 ? a.v_scale * kFp8WidenScale : 1.f;
-        Consumer<KV, C> cs;
-        cs.init(lane);
-        for (int n = 0;; ++n) {
-            const int slot = n % kQueue;
-            const bool got = mbar_wait(smem_addr(item_full + slot), (n / kQueue) & 1);
-            // one decision for all consumer warps: stop on a wait that ran out,
-            // here or in an earlier chunk, or on the producer's abort
-            if (consumer_bar_any(!got || *reinterpret_cast<volatile int*>(abort_flag) != 0)) break;
-            const Item it = desc[slot];
-            if (it.seq < 0) break;
-            const int kvh = it.grp / n_hg;
-            const int hg = it.grp - kvh * n_hg;
-            const int h0 = kvh * a.group + hg * kHeadsPerCta;
-            const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
-            cs.reset();
-            cs.template load_q<false>(reinterpret_cast<const uint16_t*>(qslots + slot * C::kQSlotBytes), nh,
-                                      a.q_dtype == PA_BF16);
-            // this warp's chunks: global chunk k belongs to warp k % 4
-            const int first = it.chunk0 + ((warp - it.chunk0) % kConsumers + kConsumers) % kConsumers;
-            for (int k = first; k < it.chunk0 + it.n_chunks; k += kConsumers) {
-                const int st = k % NSTAGES;
-                const bool landed = mbar_wait(smem_addr(full + st), (k / NSTAGES) & 1);
-                if (!__all_sync(0xffffffffu, landed)) {
-                    if (lane == 0) atomicExch(abort_flag, 1);
-                    break;
-                }
-                const uint32_t kb = ring + st * C::kStageBytes;
-                cs.chunk(kb, kb + C::kTileBytes, 0, min(kChunk, it.tok1 - (it.tok0 + (k - it.chunk0) * kChunk)), sc);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(empty + st));
-            }
-            cs.finish();
-
-            // ---- merge the four warps: each adds its output, rescaled to the
-            // merged per-head maximum, into one shared accumulator
-            if (cs.g == 0) {
-                wm[warp * kHeadsPerCta + 2 * cs.q4] = cs.m0;
-                wm[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.m1;
-                wl[warp * kHeadsPerCta + 2 * cs.q4] = cs.l0;
-                wl[warp * kHeadsPerCta + 2 * cs.q4 + 1] = cs.l1;
-            }
-            consumer_bar();
-            auto head_max = [&](int h) {
-                float M = kNegInf;
-#pragma unroll
-                for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, wm[w * kHeadsPerCta + h]);
-                return M;
-            };
-            {
-                const int ha = 2 * cs.q4, hb = ha + 1;
-                const float ca = (cs.m0 == kNegInf || ha >= nh) ? 0.f : exp2_approx(cs.m0 - head_max(ha));
-                const float cb = (cs.m1 == kNegInf || hb >= nh) ? 0.f : exp2_approx(cs.m1 - head_max(hb));
-                float* ra = acc + ha * kMergeStride;
-                float* rb = acc + hb * kMergeStride;
-                if (ca != 0.f) {
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        atomicAdd(ra + cs.d_lo(mt), cs.o[mt][0] * ca);
-                        atomicAdd(ra + cs.d_hi(mt), cs.o[mt][2] * ca);
-                    }
-                }
-                if (cb != 0.f) {
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        atomicAdd(rb + cs.d_lo(mt), cs.o[mt][1] * cb);
-                        atomicAdd(rb + cs.d_hi(mt), cs.o[mt][3] * cb);
-                    }
-                }
-            }
-            consumer_bar();
-            // Results, and the accumulator back to zero.  The next item's
-            // start barrier orders these reads before its own adds.
-            for (int i = tid; i < nh * kD; i += kConsumers * 32) {
-                const int h = i / kD, d = i - h * kD;
-                const float M = head_max(h);
-                float L = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumers; ++w) {
-                    const float mw = wm[w * kHeadsPerCta + h];
-                    L += mw == kNegInf ? 0.f : wl[w * kHeadsPerCta + h] * exp2_approx(mw - M);
-                }
-                const int64_t row = static_cast<int64_t>(it.seq) * a.num_q_heads + h0 + h;
-                store_result(a, row, d, it.part, it.n_parts, L > 0.f ? acc[h * kMergeStride + d] * vs / L : 0.f, M,
-                             L);
-                acc[h * kMergeStride + d] = 0.f;
-            }
-            if (it.n_parts > 1 && a.fused_merge) {
-                merge_group_if_last(a, it.seq, it.seq * n_grp + it.grp, h0, nh, it.n_parts, tid, kConsumers * 32,
-                                    [] { consumer_bar(); });
-            }
-            // the query slot and descriptor were read before the first merge barrier
-            if (tid == 0) mbar_arrive(smem_addr(item_empty + slot));
-        }
-    }
-
-    __syncthreads();
-    // the last CTA to finish resets the item counter for the next call
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-            sched[0] = 0;
-            sched[1] = 0;
-        }
-    }
-}
-
 // ------------------------------------------------------------ host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1040,25 +681,6 @@ pa_status launch(const DecodeArgs& a, cudaStream_t stream) {
     if (!make_pool_map(&mk, a.k_cache, a, box_rows, three_d) || !make_pool_map(&mv, a.v_cache, a, box_rows, three_d))
         return PA_ERR_CUDA;
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
-    if (a.persistent) {
-        using C = PersistCfg<KV, BS, NSTAGES>;
-        auto kernel = decode_mma_persistent_kernel<KV, BS, NSTAGES>;
-        // once per instantiation: raise its shared-memory limit, count resident CTAs per SM
-        static std::once_flag once;
-        static cudaError_t err = cudaSuccess;
-        static int per_sm = 0;
-        std::call_once(once, [&] {
-            err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-            if (err == cudaSuccess)
-                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, C::kSmemBytes);
-        });
-        if (err != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-        const int64_t items = static_cast<int64_t>(a.batch) * a.num_kv_heads * n_hg * a.max_parts;
-        const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items, int64_t(per_sm) * sm_count())));
-        if (launch_pdl(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess)
-            return PA_ERR_CUDA;
-        return PA_OK;
-    }
     using C = GridCfg<KV, BS, NSTAGES>;
     auto kernel = decode_mma_kernel<KV, BS, NSTAGES>;
     static std::once_flag once;   // once per instantiation

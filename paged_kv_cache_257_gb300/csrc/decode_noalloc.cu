@@ -59,7 +59,7 @@ extern "C" pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, con
         pa_status st = scratch_address(&ws);
         if (st != PA_OK) return st;
         // The array keeps the previous call's contents.  Its front holds the
-        // counters a call expects at zero (work scheduling and merge tickets):
+        // counters a call expects at zero (the merge tickets):
         // clear them on the caller's stream, ahead of the kernels.
         const size_t counters =
             pa::decode_counter_bytes(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);

@@ -211,11 +211,10 @@ def test_append_rejects_bad_arguments(pa):
 def test_workspace_and_partition_sizes(pa):
     d = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
     assert pa.partition_size(d, 4, 64, 8192, 512) == 512
-    # scheduler counters (256 B), merge tickets (4 x 8 groups, padded to 256 B),
-    # partial outputs, partial (max, sum)
-    assert pa.decode_workspace_size(d, 4, 64, 8192, 512) == 256 + 256 + 4 * 64 * 256 * 128 * 4 + 4 * 64 * 256 * 2 * 4
+    # merge tickets (4 x 8 groups, padded to 256 B), partial outputs, partial (max, sum)
+    assert pa.decode_workspace_size(d, 4, 64, 8192, 512) == 256 + 4 * 64 * 256 * 128 * 4 + 4 * 64 * 256 * 2 * 4
     assert pa.partition_size(d, 4, 64, 8192, -1) == 131072
-    assert pa.decode_workspace_size(d, 4, 64, 8192, -1) == 256       # scheduler counters only
+    assert pa.decode_workspace_size(d, 4, 64, 8192, -1) == 0         # no split, no workspace
     assert pa.partition_size(d, 4, 64, 8192, 100) == -1
     auto = pa.partition_size(d, 4, 64, 8192, 0)
     assert auto > 0 and auto % 16 == 0
