@@ -271,8 +271,8 @@ class GpuWorkload:
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h")
-NCU_TRAFFIC = {"c9b85a47c54a9db1": {"gqa_bf16": 283_139_840 + 3_936_512,
-                                    "longctx_fp8": 1_074_026_000 + 8_757_760}}
+NCU_TRAFFIC = {"fe88a1c3849600c7": {"gqa_bf16": 283_141_888 + 4_246_016,
+                                    "longctx_fp8": 1_074_084_000 + 8_445_440}}
 
 
 def captured_traffic(workload):
