@@ -35,6 +35,10 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2**20
 
 
+# tokens per KV block of the workload (None: its own)
+BLOCK_SIZE = None
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -45,6 +49,8 @@ def parse():
     p.add_argument("--partition", type=int, default=None, help="tokens per partition (default: the workload's)")
     p.add_argument("--window", type=int, default=0,
                    help="attend only each sequence's last W tokens (a slid window; 0: the whole context)")
+    p.add_argument("--block-size", type=int, default=None, choices=[8, 16, 32],
+                   help="re-block gqa_bf16 / mha_f16 / longctx_fp8 (default: their 16-token blocks)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle baseline sample")
     p.add_argument("--clock-probe-s", type=float, default=2.0,
@@ -135,7 +141,7 @@ class GpuWorkload:
         import paged_kv_cache_257_gb300 as pa
         from synth import workloads as wl
         self.pa, self.torch = pa, torch
-        self.w = w = wl.make(name)
+        self.w = w = wl.make(name, BLOCK_SIZE)
         self.device = device
         self.partition = w.partition_size if partition is None else partition
         bs = w.block_size
@@ -285,6 +291,33 @@ def captured_traffic(workload):
     return NCU_TRAFFIC.get(h.hexdigest()[:16], {}).get(workload)
 
 
+def copy_blocks_timing(pa, torch, w, device, pairs=4096):
+    """Copy-on-write's device half (pa_copy_blocks) on this workload's block
+    geometry: `pairs` shuffled block pairs of a scratch pool, K and V, timed
+    with CUDA events on the launching stream after a warm-up call."""
+    import synth
+    desc = pa.CacheDesc(2 * pairs, w.block_size, w.n_kv_heads, w.head_dim, w.kv_dtype, 1.0, 1.0)
+    kc, vc = desc.new_pools(device, fill=0)
+    perm = synth.permutation(92, 0, 2 * pairs).astype(np.int32)
+    src = torch.from_numpy(perm[:pairs].copy()).to(device)
+    dst = torch.from_numpy(perm[pairs:].copy()).to(device)
+    pa.copy_blocks(desc, kc, vc, src, dst)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    reps = 10
+    ev[0].record()
+    for _ in range(reps):
+        pa.copy_blocks(desc, kc, vc, src, dst)
+    ev[1].record()
+    torch.cuda.synchronize()
+    us = ev[0].elapsed_time(ev[1]) * 1e3 / reps
+    block_bytes = w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes
+    moved = 2 * pairs * block_bytes * 2          # K and V, read + write
+    del kc, vc
+    return {"pairs": pairs, "block_bytes": block_bytes, "us": us, "gbs": moved / us / 1e3,
+            "frac_of_peak": moved / us / 1e3 / measured_peak()[0],
+            "note": "pa_copy_blocks on a scratch pool (2 x pairs blocks), read + write bytes, after warm-up"}
+
+
 def prefix_cache_host_timing(pa, w):
     """Host cost of the prefix cache on this workload's shape: one request
     computes and caches the shared prefix; each of the others maps it
@@ -408,7 +441,7 @@ def oracle_setup(w_name):
     from oracle import allocator as oalloc
     from oracle import cache as ocache
     from synth import workloads as wl
-    w = wl.make(w_name)
+    w = wl.make(w_name, BLOCK_SIZE)
     if w.block_tables is None:
         tables, ctx, new_slots = wl.build_prefix_tables(w, oalloc.BlockAllocator(w.num_blocks, w.alloc_seed))
     else:
@@ -483,8 +516,9 @@ def max_over_ranks(x):
 
 
 def main():
-    global _dist
+    global _dist, BLOCK_SIZE
     args = parse()
+    BLOCK_SIZE = args.block_size
     rank, world, local = dist_env()
     if args.impl == "reference":
         if rank != 0:
@@ -500,7 +534,7 @@ def main():
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
     from synth import workloads as wl
-    w = wl.make(args.workload)
+    w = wl.make(args.workload, BLOCK_SIZE)
     # enough replicas of the caches that their total exceeds L2 several times
     per = w.num_blocks * w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes * 2
     replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
@@ -542,6 +576,7 @@ def main():
         line["unique_kv_gbs"] = wk.unique_kv_bytes * world / step_s / 1e9
     if w.prefix_len and rank == 0:
         line["prefix_cache"] = prefix_cache_host_timing(wk.pa, w)
+    line["copy_blocks"] = copy_blocks_timing(wk.pa, torch, w, device)
     if rank == 0 and not args.no_cpu_baseline:
         v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds, args.window)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
@@ -556,7 +591,7 @@ def main():
 def run_reference(args):
     """The oracle as the reference arm: K timed steps, each a bounded sample of the workload."""
     from synth import workloads as wl
-    w = wl.make(args.workload)
+    w = wl.make(args.workload, BLOCK_SIZE)
     per_step = max(1.0, min(10.0, 60.0 / max(1, args.steps)))
     for _ in range(args.warmup):
         oracle_step_sample(args.workload, 0.0, args.window)

@@ -95,26 +95,34 @@ def _shuffled_tables(seed, ctx, bs, num_blocks, max_blocks):
     return tables
 
 
-def make(name):
-    """The workload called ``name`` (small metadata only; values are drawn lazily)."""
+def make(name, block_size=None):
+    """The workload called ``name`` (small metadata only; values are drawn lazily).
+
+    ``block_size`` (8, 16 or 32) re-blocks the gqa_bf16, mha_f16 and
+    longctx_fp8 workloads; token values, context lengths and pool bytes stay
+    the same (the default is their 16-token blocks)."""
     seed = NAMES.index(name)
+    if block_size not in (None, 16) and name not in ("gqa_bf16", "mha_f16", "longctx_fp8"):
+        raise ValueError(f"{name} has 16-token blocks only")
+    bs_x = block_size or 16
     if name == "tiny":
         ctx = np.array([5, 17, 33, 64], dtype=np.int32)
         return Workload(name, seed, 4, 4, 2, 64, 16, "f32", "f32", 1.0 / 8.0, 0, ctx, 32,
                         _shuffled_tables(seed, ctx, 16, 32, 4), 4)
     if name == "gqa_bf16":
-        b, bs = 32, 16
+        b, bs = 32, bs_x
         ctx = uniform_int(seed, _stream(S_CTX), b, 1, 4096).astype(np.int32)
         used = sum(-(-int(c) // bs) for c in ctx)
-        nb = used + 32
+        nb = used + 32 * 16 // bs
         return Workload(name, seed, b, 32, 8, 128, bs, "bf16", "bf16", 1 / math.sqrt(128), 0,
-                        ctx, nb, _shuffled_tables(seed, ctx, bs, nb, 256), 256,
+                        ctx, nb, _shuffled_tables(seed, ctx, bs, nb, 4096 // bs), 4096 // bs,
                         append_tokens=32)
     if name == "mha_f16":
-        b, bs = 8, 16
+        b, bs = 8, bs_x
         ctx = np.full(b, 4096, dtype=np.int32)
+        nb = b * 4096 // bs
         return Workload(name, seed, b, 40, 40, 128, bs, "f16", "f16", 1 / math.sqrt(128), 0,
-                        ctx, 2048, _shuffled_tables(seed, ctx, bs, 2048, 256), 256)
+                        ctx, nb, _shuffled_tables(seed, ctx, bs, nb, 4096 // bs), 4096 // bs)
     if name == "prefix_bf16":
         b, bs, prefix = 64, 16, 2048
         suffix = uniform_int(seed, _stream(S_SUFFIX), b, 1, 512)
@@ -126,7 +134,7 @@ def make(name):
                         ctx, nb, None, max_blocks, append_tokens=b, prefix_len=prefix,
                         alloc_seed=0xC0FFEE)
     if name == "longctx_fp8":
-        b, bs, c = 4, 16, 131072
+        b, bs, c = 4, bs_x, 131072
         ctx = np.full(b, c, dtype=np.int32)
         nb = b * c // bs
         return Workload(name, seed, b, 64, 8, 128, bs, "fp8_e4m3", "bf16", 1 / math.sqrt(128),
