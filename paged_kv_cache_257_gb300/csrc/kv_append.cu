@@ -40,42 +40,52 @@ __device__ __forceinline__ void load_pack_f32(const void* base, int64_t elem, fl
     }
 }
 
+// One pack in registers, already in the cache's type: load() reads (and
+// converts) the source, store() writes the slot; split so that the source
+// read need not wait for the slot.
 template <pa_dtype SRC, pa_dtype DST>
-__device__ __forceinline__ void move_pack(const void* src, int64_t src_elem, void* dst, int64_t dst_elem,
-                                          float scale) {
-    if constexpr (SRC == DST) {
-        using T = typename Elem<DST>::type;
-        const uint4* s = reinterpret_cast<const uint4*>(static_cast<const T*>(src) + src_elem);
-        uint4* d = reinterpret_cast<uint4*>(static_cast<T*>(dst) + dst_elem);
-        constexpr int n16 = kPack * Elem<DST>::bytes / 16;
+struct Pack {
+    static constexpr int kWords = kPack * Elem<DST>::bytes / 4;
+    alignas(16) uint32_t w[kWords];
+
+    __device__ __forceinline__ void load(const void* src, int64_t src_elem, float scale) {
+        if constexpr (SRC == DST) {
+            using T = typename Elem<DST>::type;
+            const uint4* s = reinterpret_cast<const uint4*>(static_cast<const T*>(src) + src_elem);
 #pragma unroll
-        for (int i = 0; i < n16; ++i) d[i] = __ldg(s + i);
-    } else if constexpr (DST == PA_FP8_E4M3) {
-        float x[kPack];
-        load_pack_f32<SRC>(src, src_elem, x);
-        uint32_t w[2];
+            for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<uint4*>(w)[i] = __ldg(s + i);
+        } else if constexpr (DST == PA_FP8_E4M3) {
+            float x[kPack];
+            load_pack_f32<SRC>(src, src_elem, x);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            uint32_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(__fdiv_rn(x[4 * i + 0], scale), __fdiv_rn(x[4 * i + 1], scale)), __NV_SATFINITE,
-                __NV_E4M3);
-            uint32_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale)), __NV_SATFINITE,
-                __NV_E4M3);
-            w[i] = (lo & 0xFFFFu) | (hi << 16);
+            for (int i = 0; i < 2; ++i) {
+                uint32_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(x[4 * i + 0], scale), __fdiv_rn(x[4 * i + 1], scale)), __NV_SATFINITE,
+                    __NV_E4M3);
+                uint32_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale)), __NV_SATFINITE,
+                    __NV_E4M3);
+                w[i] = (lo & 0xFFFFu) | (hi << 16);
+            }
+        } else {
+            static_assert(SRC == PA_F32, "only float32 sources narrow to 16-bit caches");
+            float x[kPack];
+            load_pack_f32<SRC>(src, src_elem, x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = pack2<DST == PA_BF16>(x[2 * i], x[2 * i + 1]);
         }
-        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + dst_elem) = make_uint2(w[0], w[1]);
-    } else {
-        static_assert(SRC == PA_F32, "only float32 sources narrow to 16-bit caches");
-        float x[kPack];
-        load_pack_f32<SRC>(src, src_elem, x);
-        uint4 out;
-        uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = pack2<DST == PA_BF16>(x[2 * i], x[2 * i + 1]);
-        *reinterpret_cast<uint4*>(static_cast<typename Elem<DST>::type*>(dst) + dst_elem) = out;
     }
-}
+
+    __device__ __forceinline__ void store(void* dst, int64_t dst_elem) const {
+        uint8_t* d = static_cast<uint8_t*>(dst) + dst_elem * Elem<DST>::bytes;
+        if constexpr (kWords == 2) {
+            *reinterpret_cast<uint2*>(d) = make_uint2(w[0], w[1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kWords / 4; ++i) reinterpret_cast<uint4*>(d)[i] = reinterpret_cast<const uint4*>(w)[i];
+        }
+    }
+};
 
 template <pa_dtype SRC, pa_dtype DST>
 __global__ void __launch_bounds__(kAppendThreads)
@@ -97,16 +107,15 @@ kv_append_kernel(const void* __restrict__ k, const void* __restrict__ v, const i
         const int64_t t = row / num_kv_heads;
         const int64_t h = row - t * num_kv_heads;
         const int64_t slot = __ldg(slots + t);
+        Pack<SRC, DST> pk;
+        pk.load(is_v ? v : k, row * head_dim + chunk * kPack, is_v ? v_scale : k_scale);
         if (slot < 0 || slot >= num_slots) {
             if (!is_v && h == 0 && chunk == 0) raise_flag(status, PA_DEVFLAG_SLOT_RANGE);
             continue;
         }
         const int64_t blk = slot / block_size;
         const int64_t off = slot - blk * block_size;
-        const int64_t dst_elem = ((blk * num_kv_heads + h) * block_size + off) * head_dim + chunk * kPack;
-        const int64_t src_elem = row * head_dim + chunk * kPack;
-        move_pack<SRC, DST>(is_v ? v : k, src_elem, is_v ? v_cache : k_cache, dst_elem,
-                            is_v ? v_scale : k_scale);
+        pk.store(is_v ? v_cache : k_cache, ((blk * num_kv_heads + h) * block_size + off) * head_dim + chunk * kPack);
     }
 }
 
