@@ -515,8 +515,25 @@ def max_over_ranks(x):
     return float(t.item())
 
 
+def init_distributed(world):
+    """One process per GPU: a gloo group for the barrier and the max over
+    ranks (the replicas exchange no data)."""
+    global _dist
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        _dist = dist
+
+
+def job_rate(units_per_step, steps, world, local_ms):
+    """Whole-job rate: every rank's units over the slowest rank's time.
+    Returns (units per second, that time in ms)."""
+    t = max_over_ranks(local_ms)
+    return units_per_step * steps * world / (t / 1e3), t
+
+
 def main():
-    global _dist, BLOCK_SIZE
+    global BLOCK_SIZE
     args = parse()
     BLOCK_SIZE = args.block_size
     rank, world, local = dist_env()
@@ -524,10 +541,7 @@ def main():
         if rank != 0:
             return 0
         return run_reference(args)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
-        _dist = dist
+    init_distributed(world)
     import torch
     from paged_kv_cache_257_gb300 import build
     build.build()
@@ -542,10 +556,8 @@ def main():
     with ClockSampler(local) as clk:
         total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
     e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
-    total_ms = max_over_ranks(total_ms)
-    e2e_ms = max_over_ranks(e2e_ms)
-    value = w.batch * args.steps * world / (total_ms / 1e3)
-    e2e_value = w.batch * args.steps * world / (e2e_ms / 1e3)
+    value, total_ms = job_rate(w.batch, args.steps, world, total_ms)
+    e2e_value, e2e_ms = job_rate(w.batch, args.steps, world, e2e_ms)
     dec_avg_s = statistics.mean(dec_ms) / 1e3
     peak, peak_src = measured_peak()
     achieved = wk.kv_bytes / dec_avg_s / 1e9
