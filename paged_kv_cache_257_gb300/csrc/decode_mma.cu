@@ -76,56 +76,23 @@ struct Cfg {
 #define PA_DECODE_STAGES_FP8 8
 #endif
 
-// How FP8 tiles are widened to float16 for the tensor cores.
-//  0: cvt.rn.f16x2.e4m3x2 on pairs of codes (exact values).  The default: on
-//     the long-context FP8 workload it ran 242 us against 273 us for 1.
-//  1: move bit fields.  A float16 holding an E4M3 code's sign, exponent and
-//     mantissa bits in place (exponent bias 15 instead of 7) equals the E4M3
-//     value times 2^-8, subnormals included, so the scales absorb 2^8.  Four
-//     codes take 7 integer operations and no byte permute.
-#ifndef PA_FP8_WIDEN_BITS
-#define PA_FP8_WIDEN_BITS 0
-#endif
-constexpr float kFp8WidenScale = PA_FP8_WIDEN_BITS ? 256.f : 1.f;
-
-#if PA_FP8_WIDEN_BITS
-// codes 0, 2 -> `even` (low, high half), codes 1, 3 -> `odd`; values x 2^-8
-__device__ __forceinline__ void e4m3_fields_to_f16(uint32_t x, uint32_t& even, uint32_t& odd) {
-    odd = (x & 0x80008000u) | ((x >> 1) & 0x3F803F80u);
-    even = ((x << 8) & 0x80008000u) | ((x << 7) & 0x3F803F80u);
-}
-#endif
+// FP8 tiles are widened to float16 for the tensor cores with
+// cvt.rn.f16x2.e4m3x2 on pairs of codes (exact values).  Moving the E4M3 bit
+// fields into float16 positions instead (values x 2^-8, folded into the
+// scales; 7 integer operations per four codes, no byte permute) ran 273 us
+// against 242 us on the long-context FP8 workload.
 
 // K operand: the four codes a thread holds of one row (d+0..3) as the A
-// fragment's (k 2q, 2q+1) and (k 2q+8, 2q+9) registers.  Which d lands in
-// which k is matched by the query permutation in fp8_q_pairs.
+// fragment's (k 2q, 2q+1) and (k 2q+8, 2q+9) registers; the query is loaded
+// in the same d order.
 __device__ __forceinline__ void fp8_k_pairs(uint32_t x, uint32_t& k01, uint32_t& k89) {
-#if PA_FP8_WIDEN_BITS
-    e4m3_fields_to_f16(x, k01, k89);          // d+{0,2} | d+{1,3}
-#else
     e4m3x4_to_f16x2x2(x, k01, k89);           // d+{0,1} | d+{2,3}
-#endif
-}
-
-// The query's float16 values at d+0..3 (h0..h3) in the same k order.
-__device__ __forceinline__ void fp8_q_pairs(uint32_t h01, uint32_t h23, uint32_t& k01, uint32_t& k89) {
-#if PA_FP8_WIDEN_BITS
-    k01 = __byte_perm(h01, h23, 0x5410);      // h0, h2
-    k89 = __byte_perm(h01, h23, 0x7632);      // h1, h3
-#else
-    k01 = h01;
-    k89 = h23;
-#endif
 }
 
 // V operand: an ldmatrix.trans register (token 2q: d, d+1 | token 2q+1: d, d+1)
 // as the token pairs at d and at d+1.
 __device__ __forceinline__ void fp8_v_pairs(uint32_t x, uint32_t& at_d, uint32_t& at_d1) {
-#if PA_FP8_WIDEN_BITS
-    e4m3_fields_to_f16(x, at_d, at_d1);
-#else
     e4m3x4_to_f16x2x2(__byte_perm(x, 0, 0x3120), at_d, at_d1);
-#endif
 }
 
 // Largest growth (log2 units) of a chunk's score maximum over the running
@@ -236,7 +203,8 @@ struct Consumer {
                     h01 = pack2<false>(__uint_as_float(h01 << 16), __uint_as_float(h01 & 0xffff0000u));
                     h23 = pack2<false>(__uint_as_float(h23 << 16), __uint_as_float(h23 & 0xffff0000u));
                 }
-                fp8_q_pairs(h01, h23, qf[kk][0], qf[kk][1]);   // ordered like fp8_k_pairs
+                qf[kk][0] = h01;   // d+0, d+1: ordered like fp8_k_pairs
+                qf[kk][1] = h23;   // d+2, d+3
             }
         }
     }
@@ -554,7 +522,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         drain_ring<NSTAGES>(a, full, issued, lane);
     } else {
         // ------------------------------------------------------ consumers
-        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale * kFp8WidenScale : 1.f);
+        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
         cs.convert_q(a.q_dtype == PA_BF16);
         for (int c = warp; c < n_chunks; c += kConsumers) {
             const int st = c % NSTAGES;
@@ -600,7 +568,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     if (threadIdx.x < kD) {
         const int d = threadIdx.x;
-        const float vs = kFp8 ? a.v_scale * kFp8WidenScale : 1.f;
+        const float vs = kFp8 ? a.v_scale : 1.f;
         for (int h = 0; h < nh; ++h) {
             float M = kNegInf;
 #pragma unroll
