@@ -12,16 +12,18 @@
 // warp:
 //   * the producer walks the item's block table (32 ids per coalesced load)
 //     and streams each 16-token chunk's K and V tiles into a ring of shared
-//     memory stages with 2-D TMA loads (128-byte swizzle, evict-first L2
-//     hint), arming an mbarrier per stage;
+//     memory stages with TMA loads (128-byte swizzle, evict-first L2 hint;
+//     one 3-D box per 16-bit tile), arming an mbarrier per stage;
 //   * the consumer warp owning a chunk forms S^T = K Q^T with mma.sync
 //     m16n8k16 (16 tokens x 8 heads, heads on the N side so G = 8 needs no
 //     padding), runs the online softmax in registers, turns P into the B
 //     operand with two movmatrix transposes and accumulates O^T = V^T P^T;
 //   * the warps' (max, sum, output) states are merged and written as the
 //     final output or, for a split context, as a partition partial.
-// The grid runs one CTA per item.  FP8 tiles are widened to float16 in registers, with the K scale folded into
-// the score scale and the V scale into the output.
+// The grid runs one CTA per item, 5 resident per SM.  FP8 tiles are widened
+// to float16 in registers, with the K scale folded into the score scale and
+// the V scale into the output.  A slid window ([start, ctx) of the row) masks
+// the positions of its first chunk that precede the start.
 #include <algorithm>
 #include <mutex>
 
