@@ -387,7 +387,12 @@ def time_device(wk, steps, warmup, probe_s=0.0):
 
 
 def time_e2e(wk, steps, warmup):
-    """The public API from pinned host buffers: H2D of the step inputs, the step, D2H of the output."""
+    """The public API from pinned host buffers, as a serving loop drives it:
+    every step uploads its inputs and downloads its output.  The uploads and
+    downloads run on their own streams into two sets of buffers, so the next
+    step's inputs and the previous step's output move while this step
+    computes; a buffer is reused only after the step two back has finished
+    with it.  The timed region ends when the last output is in host memory."""
     torch, pa = wk.torch, wk.pa
     host = {"q": wk.q.cpu().pin_memory(), "bt": wk.block_tables.cpu().pin_memory(),
             "ctx": wk.context_lens.cpu().pin_memory()}
@@ -396,21 +401,56 @@ def time_e2e(wk, steps, warmup):
     if wk.new_k is not None:
         host.update(k=wk.new_k.cpu().pin_memory(), v=wk.new_v.cpu().pin_memory(),
                     slots=wk.new_slots.cpu().pin_memory())
-    out_host = torch.empty(wk.out.shape, dtype=wk.out.dtype).pin_memory()
-    dev = {k: torch.empty_like(v, device=wk.device) for k, v in host.items()}
+    out_host = [torch.empty(wk.out.shape, dtype=wk.out.dtype).pin_memory() for _ in range(2)]
+    outs = [torch.empty_like(wk.out) for _ in range(2)]
+    # every input of a step in one pinned staging buffer (256-byte aligned
+    # pieces), so a step uploads with one copy; typed views on each side
+    offs, size = {}, 0
+    for k, v in host.items():
+        offs[k] = size
+        size += (v.numel() * v.element_size() + 255) // 256 * 256
+    stage = torch.empty(size, dtype=torch.uint8).pin_memory()
+    for k, v in host.items():
+        n = v.numel() * v.element_size()
+        stage[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
+    bufs = [torch.empty(size, dtype=torch.uint8, device=wk.device) for _ in range(2)]
+
+    def views(buf):
+        return {k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                for k, v in host.items()}
+
+    dev = [views(buf) for buf in bufs]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    computed = [torch.cuda.Event() for _ in range(2)]     # step done with dev[b], outs[b] written
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):
+        computed[b].record(comp)
+        downloaded[b].record(comp)
 
     def one(r):
-        for k, v in host.items():
-            dev[k].copy_(v, non_blocking=True)
+        b = r % 2
+        with torch.cuda.stream(up):
+            up.wait_event(computed[b])
+            bufs[b].copy_(stage, non_blocking=True)
+            uploaded[b].record(up)
+        comp.wait_event(uploaded[b])
+        comp.wait_event(downloaded[b])
         kc, vc = wk.pools[r % len(wk.pools)]
-        if "k" in dev:
-            pa.kv_append(wk.desc, dev["k"], dev["v"], dev["slots"], kc, vc)
+        d = dev[b]
+        if "k" in d:
+            pa.kv_append(wk.desc, d["k"], d["v"], d["slots"], kc, vc)
         part = wk.plan_partition() if wk.plan else wk.partition   # host work of a serving step
-        pa.decode_attention(wk.desc, dev["q"], kc, vc, dev["bt"], dev["ctx"], wk.w.scale,
-                            partition=part, workspace=wk.workspace, out=wk.out, context_starts=dev.get("starts"))
-        out_host.copy_(wk.out, non_blocking=True)
+        pa.decode_attention(wk.desc, d["q"], kc, vc, d["bt"], d["ctx"], wk.w.scale,
+                            partition=part, workspace=wk.workspace, out=outs[b], context_starts=d.get("starts"))
+        computed[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(computed[b])
+            out_host[b].copy_(outs[b], non_blocking=True)
+            downloaded[b].record(down)
 
     for i in range(warmup):
         one(i)
@@ -418,10 +458,12 @@ def time_e2e(wk, steps, warmup):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    start.record()
+    start.record(comp)
+    up.wait_event(start)
     for i in range(steps):
         one(warmup + i)
-    end.record()
+    comp.wait_event(downloaded[(warmup + steps - 1) % 2])
+    end.record(comp)
     torch.cuda.synchronize()
     return start.elapsed_time(end), h2d, d2h
 

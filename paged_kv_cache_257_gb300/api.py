@@ -32,8 +32,14 @@ class CacheDesc:
     v_scale: float = 1.0
 
     def c(self):
-        return _native.CacheDescC(self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim,
-                                  DTYPE[self.kv_dtype], self.k_scale, self.v_scale)
+        """The C struct (built once per distinct field values: calls are on the hot path)."""
+        key = (self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim, self.kv_dtype, self.k_scale,
+               self.v_scale)
+        if self.__dict__.get("_c_key") != key:
+            self.__dict__["_c"] = _native.CacheDescC(self.num_blocks, self.block_size, self.num_kv_heads,
+                                                     self.head_dim, DTYPE[self.kv_dtype], self.k_scale, self.v_scale)
+            self.__dict__["_c_key"] = key
+        return self.__dict__["_c"]
 
     @property
     def pool_shape(self):
@@ -158,7 +164,8 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
 
     ``q`` is ``[batch, num_q_heads, head_dim]``; ``block_tables`` int32
     ``[batch, max_blocks]``; ``context_lens`` int32 ``[batch]``.  ``out`` and
-    the split-context ``workspace`` are allocated with torch when not given.
+    the split-context ``workspace`` are allocated with torch when not given; a
+    given workspace is passed with its size, which the library checks.
     ``context_starts`` (device int32 ``[batch]``) restricts each sequence to
     the positions from its start on (``pa_decode_attention_window``).
     """
@@ -176,9 +183,10 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
         out = torch.empty((batch, hq, d), dtype=TORCH_STORAGE[od], device=q.device)
     _need(out, "out")
     od = _dtype_of(out, "out")
-    need = decode_workspace_size(desc, batch, hq, max_blocks, partition)
-    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
-        workspace = new_workspace(need, q.device)
+    if workspace is None:
+        need = decode_workspace_size(desc, batch, hq, max_blocks, partition)
+        workspace = new_workspace(need, q.device) if need else None
+    need = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = desc.c()
     if context_starts is None:
         st = lib().pa_decode_attention(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),
