@@ -196,9 +196,13 @@ size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32
  * (attention formula), section 2 Example 2 (grouped-query heads), section 4
  * "The PagedAttention CUDA Kernel" (read the query, look up the block table,
  * fetch K and V from scattered blocks).  Long contexts are split into
- * partitions of `partition_size` tokens whose partial results are merged by
- * log-sum-exp: by the last partition's CTA when a sequence has at most 16
- * partitions, otherwise by a second kernel.
+ * partitions of at most `partition_size` tokens whose partial results are
+ * merged by log-sum-exp: by the last partition's CTA when a sequence has at
+ * most 16 partitions, otherwise by a second kernel.  A sequence of len tokens
+ * splits into n = ceil(len / partition_size) partitions of equal share
+ * (ceil(len / n) rounded up to 16 tokens, or to the block size if larger),
+ * so the work items of a ragged batch stay alike in size; a length that is a
+ * multiple of partition_size gives partitions of exactly that size.
  *   q              device [batch][num_q_heads][head_dim] of q_dtype
  *   block_tables   device [batch][max_blocks_per_seq] int32
  *   context_lens   device [batch] int32, cached tokens per sequence (0 gives

@@ -59,23 +59,31 @@ int32_t plan_partition(const pa_cache_desc* c, int32_t batch, int32_t num_q_head
     const int64_t per_seq = static_cast<int64_t>(c->num_kv_heads) * groups;
     const int64_t slots = static_cast<int64_t>(PA_DECODE_MIN_CTAS) * std::max(num_sms, 1);
     const int64_t whole = std::max<int64_t>((cap + unit - 1) / unit * unit, unit);
-    int64_t longest = 0;
-    for (int32_t s = 0; s < batch; ++s)
-        longest = std::max<int64_t>(longest, lens ? std::min<int64_t>(std::max(lens[s], 0), cap) : cap);
-    auto items_for = [&](int64_t p) {
-        int64_t n = 0;
+    // items (partitions x head groups) and the longest partition share for a
+    // partition size p: a sequence of len tokens splits into ceil(len / p)
+    // equal shares, each rounded up to the unit
+    auto model = [&](int64_t p, int64_t& items, int64_t& longest) {
+        items = 0;
+        longest = 0;
         for (int32_t s = 0; s < batch; ++s) {
-            const int64_t ctx = lens ? std::min<int64_t>(std::max(lens[s], 0), cap) : cap;
-            n += (ctx + p - 1) / p;
+            const int64_t len = lens ? std::min<int64_t>(std::max(lens[s], 0), cap) : cap;
+            if (len == 0) continue;
+            const int64_t n = (len + p - 1) / p;
+            const int64_t share = ((len + n - 1) / n + unit - 1) / unit * unit;
+            items += n;
+            longest = std::max(longest, std::min(share, len));
         }
-        return n * per_seq;
+        items *= per_seq;
     };
+    int64_t items = 0, longest = 0;
+    model(whole, items, longest);
     int64_t best = whole;
-    int64_t best_cost = plan_cost(items_for(whole), std::min(whole, longest), slots);
+    int64_t best_cost = plan_cost(items, longest, slots);
     const int32_t cands[] = {8192, 4096, 2048, 1024, 512, 256};
     for (int32_t p : cands) {
         if (p % unit != 0 || p >= whole) continue;
-        const int64_t cost = plan_cost(items_for(p), std::min<int64_t>(p, longest), slots);
+        model(p, items, longest);
+        const int64_t cost = plan_cost(items, longest, slots);
         if (cost < best_cost) {
             best = p;
             best_cost = cost;

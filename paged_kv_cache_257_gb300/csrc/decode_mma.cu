@@ -458,8 +458,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     pdl_trigger();
     // The context length, the partition's first block ids and the query do
     // not depend on one another: issue all three loads before waiting on
-    // any, so a CTA's first copy waits for one round trip less.  Without
-    // window starts a partition's blocks begin at part * P / block_size.
+    // any, so a CTA's first copy waits for one round trip less.  The ids are
+    // a guess (blocks from part * P / block_size, right without window starts
+    // when the partition share is P, and always for partition 0), used only
+    // once the real start confirms it.
     Consumer<KV, C> cs;
     cs.init(lane);
     cs.reset();
@@ -479,8 +481,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
-    const int tok0 = sw.tok0(part, a.partition_size);
-    const int tok1 = sw.tok1(part, a.partition_size);
+    const int tok0 = sw.tok0(part);
+    const int tok1 = sw.tok1(part);
     const int lead = sw.lead(part);   // positions of chunk 0 before the window
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
 
@@ -498,7 +500,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         // ------------------------------------------------------ producer
         const uint64_t policy = l2_evict_first_policy();
         BlockWindow win;
-        if (spec)
+        if (spec && tok0 == part * a.partition_size)
             win.start_loaded(bt_row, tok0, tok1, BS, spec_ids);
         else
             win.start(bt_row, tok0, tok1, BS);

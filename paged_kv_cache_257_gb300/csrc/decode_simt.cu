@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
     const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
-    const int tok0 = sw.tok0(part, a.partition_size);
-    const int tok1 = sw.tok1(part, a.partition_size);
+    const int tok0 = sw.tok0(part);
+    const int tok1 = sw.tok1(part);
     const int h0 = kvh * a.group + hg * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
     const float sc = a.scale * 1.4426950408889634f;
