@@ -17,6 +17,7 @@ streams its KV from HBM.
 
 import argparse
 import json
+import platform
 import math
 import os
 import statistics
@@ -32,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode-attn tokens/s and KV HBM GB/s (fraction of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0   # HBM3e nominal bandwidth of one GB300 (about 8 TB/s)
 L2_BYTES = 129 * 2**20
 
 
@@ -218,6 +220,9 @@ class GpuWorkload:
         self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=torch.float32, device=device)
         self.resolved_partition = pa.partition_size(self.desc, w.batch, w.n_q_heads, self.tables_np.shape[1],
                                                     self.partition)
+        # the merge kernel runs when a sequence may hold more than 16 partitions
+        cap = self.tables_np.shape[1] * bs
+        self.merge_launches = 1 if -(-cap // self.resolved_partition) > 16 else 0
 
     def alloc_tables(self, wl):
         w = self.w
@@ -253,21 +258,27 @@ class GpuWorkload:
             return None, None, None
         return dev(k), dev(v), torch.from_numpy(np.asarray(slots, dtype=np.int64)).to(self.device)
 
-    def step(self, r, decode_events=None):
+    def step(self, r, ev=None):
+        """One step on cache replica r; ``ev``: None or four events (append
+        start, end, decode start, end).  Returns the kernels it launched."""
         pa = self.pa
         kc, vc = self.pools[r % len(self.pools)]
         n = 0
         if self.new_k is not None:
+            if ev is not None:
+                ev[0].record()
             pa.kv_append(self.desc, self.new_k, self.new_v, self.new_slots, kc, vc)
+            if ev is not None:
+                ev[1].record()
             n += 1
-        if decode_events is not None:
-            decode_events[0].record()
+        if ev is not None:
+            ev[2].record()
         pa.decode_attention(self.desc, self.q, kc, vc, self.block_tables, self.context_lens, self.w.scale,
                             partition=self.partition, workspace=self.workspace, out=self.out,
                             context_starts=self.context_starts)
-        if decode_events is not None:
-            decode_events[1].record()
-        return n + 1 + (1 if self.workspace is not None else 0)
+        if ev is not None:
+            ev[3].record()
+        return n + 1 + self.merge_launches
 
 
 # DRAM bytes (read + write) of one decode_mma_kernel launch, from the ncu
@@ -356,7 +367,10 @@ def prefix_cache_host_timing(pa, w):
 
 
 def time_device(wk, steps, warmup, probe_s=0.0):
-    """Timed region: barrier + synchronize, K steps, synchronize; per-decode events too.
+    """Timed region: barrier + synchronize, K steps, synchronize.  Then K
+    more steps with events around the append and the decode.  Returns (total
+    ms of the timed region, decode ms per step, append ms per step or [],
+    launches in the timed region).
 
     ``probe_s`` seconds of extra untimed steps run first so that the clock
     sampler (nvidia-smi, 200 ms period) sees the GPU under this load."""
@@ -371,19 +385,41 @@ def time_device(wk, steps, warmup, probe_s=0.0):
         if i % 256 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
-    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     launches = 0
     start.record()
     for i in range(steps):
-        launches += wk.step(warmup + i, dec[i])
+        launches += wk.step(warmup + i)
     end.record()
     torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
-    dec_ms = [a.elapsed_time(b) for a, b in dec]
-    return total_ms, dec_ms, launches
+    # the same steps again with events around each kernel, for per-kernel
+    # durations (the events add time between kernels, so not in the total)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        wk.step(warmup + i, ev[i])
+    torch.cuda.synchronize()
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    app_ms = [e[0].elapsed_time(e[1]) for e in ev] if wk.new_k is not None else []
+    return total_ms, dec_ms, app_ms, launches
+
+
+def time_decode_no_flush(wk, steps):
+    """Decode durations with one cache replica reused step after step (its
+    KV stays in L2 as far as it fits), after a warm-up step."""
+    torch = wk.torch
+    wk.step(0)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        wk.step(0, ev[i])
+    torch.cuda.synchronize()
+    return [e[2].elapsed_time(e[3]) for e in ev]
+
+
+def _stats_us(ms):
+    return {"mean": statistics.mean(ms) * 1e3, "median": statistics.median(ms) * 1e3, "min": min(ms) * 1e3}
 
 
 def time_e2e(wk, steps, warmup):
@@ -529,6 +565,21 @@ def oracle_step_sample(w_name, budget_s, window=0):
     return done / dt, done, dt, sample
 
 
+def host_cpu():
+    """The host's CPU model and logical core count."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count()}
+
+
 def oracle_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -596,7 +647,8 @@ def main():
     replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
     wk = GpuWorkload(args.workload, device, replicas, args.partition, args.window)
     with ClockSampler(local) as clk:
-        total_ms, dec_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
+        total_ms, dec_ms, app_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
+    no_flush_ms = time_decode_no_flush(wk, args.steps)
     e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
     value, total_ms = job_rate(w.batch, args.steps, world, total_ms)
     e2e_value, e2e_ms = job_rate(w.batch, args.steps, world, e2e_ms)
@@ -618,23 +670,28 @@ def main():
         "kv_tokens_per_s": wk.kv_tokens * world / step_s,
         "kv_gbs": wk.kv_bytes * world / step_s / 1e9,
         "decode_kernel_us": dec_avg_s * 1e6,
+        "decode_us": dict(_stats_us(dec_ms), no_flush_median=statistics.median(no_flush_ms) * 1e3,
+                          no_flush_note="one replica reused: its KV stays in L2 as far as it fits"),
         "roofline": {"bound": "hbm", "kernel": "paged decode (decode + split merge)", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": captured_traffic(args.workload), "traffic_of": "one decode_mma_kernel launch (ncu)",
-                     "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes},
+                     "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes,
+                     "nominal_peak_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": dict(clk.summary(), window=f"{args.clock_probe_s:.1f} s of the same steps + the timed steps"),
     }
     if wk.unique_kv_bytes != wk.kv_bytes:
         line["unique_kv_gbs"] = wk.unique_kv_bytes * world / step_s / 1e9
+    if app_ms:
+        line["append_us"] = dict(_stats_us(app_ms), tokens=w.append_tokens)
     if w.prefix_len and rank == 0:
         line["prefix_cache"] = prefix_cache_host_timing(wk.pa, w)
     line["copy_blocks"] = copy_blocks_timing(wk.pa, torch, w, device)
     if rank == 0 and not args.no_cpu_baseline:
         v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds, args.window)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-                                "sample": sample}
+                                "sample": sample, **host_cpu()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if _dist is not None:
@@ -665,7 +722,7 @@ def run_reference(args):
                        "kv_dtype": w.kv_dtype, "parallelism": "host cores",
                        **({"window": args.window} if args.window > 0 else {})},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
