@@ -288,8 +288,8 @@ class GpuWorkload:
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h")
-NCU_TRAFFIC = {"fe88a1c3849600c7": {"gqa_bf16": 283_141_888 + 4_246_016,
-                                    "longctx_fp8": 1_074_084_000 + 8_445_440}}
+NCU_TRAFFIC = {"7488f04de310508e": {"gqa_bf16": 283_142_144 + 3_683_072,
+                                    "longctx_fp8": 1_074_026_000 + 8_595_968}}
 
 
 def captured_traffic(workload):
