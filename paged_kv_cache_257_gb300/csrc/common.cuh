@@ -100,6 +100,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // Make barrier initialisation visible to the async (TMA) proxy.
+// Order this thread's earlier generic-proxy accesses to shared memory (say
+// ldmatrix reads of a stage) before later async-proxy ones (a TMA copy into it).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

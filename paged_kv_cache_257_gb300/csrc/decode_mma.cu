@@ -8,16 +8,17 @@
 // heads share one KV head (query head h reads KV head h / G).
 //
 // A work item is one (sequence, KV head, group of up to 8 of its query heads,
-// partition of the context).  A CTA has four consumer warps and one producer
-// warp:
-//   * the producer walks the item's block table (32 ids per coalesced load)
-//     and streams each 16-token chunk's K and V tiles into a ring of shared
-//     memory stages with TMA loads (128-byte swizzle, evict-first L2 hint;
-//     one 3-D box per 16-bit tile), arming an mbarrier per stage;
-//   * the consumer warp owning a chunk forms S^T = K Q^T with mma.sync
-//     m16n8k16 (16 tokens x 8 heads, heads on the N side so G = 8 needs no
-//     padding), runs the online softmax in registers, turns P into the B
-//     operand with two movmatrix transposes and accumulates O^T = V^T P^T;
+// partition of the context).  A CTA has four warps; chunk k of the item (16
+// tokens) belongs to warp k % 4 and to ring stage k % NSTAGES, which only
+// that warp uses:
+//   * the warp walks the item's block table (32 ids per coalesced load) and
+//     streams its chunks' K and V tiles into its stages with TMA loads
+//     (128-byte swizzle, evict-first L2 hint; one 3-D box per 16-bit tile),
+//     arming an mbarrier per stage, NSTAGES / 4 chunks ahead;
+//   * for each chunk it forms S^T = K Q^T with mma.sync m16n8k16 (16 tokens
+//     x 8 heads, heads on the N side so G = 8 needs no padding), runs the
+//     online softmax in registers, turns P into the B operand with two
+//     movmatrix transposes and accumulates O^T = V^T P^T;
 //   * the warps' (max, sum, output) states are merged and written as the
 //     final output or, for a split context, as a partition partial.
 // The grid runs one CTA per item, 5 resident per SM.  FP8 tiles are widened
@@ -37,8 +38,8 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kChunk = 16;        // tokens per mma row tile
-constexpr int kConsumers = 4;     // consumer warps
-constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kConsumers = 4;     // warps per CTA, each consuming (and loading) its own stages
+constexpr int kThreads = kConsumers * 32;
 constexpr int kMergeStride = kD + 4;  // floats per head row in merge buffers (bank spread)
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -61,7 +62,7 @@ struct Cfg {
     static constexpr int kRingBytes = NSTAGES * kStageBytes;
     static constexpr bool k3D = PA_TMA_3D && kHalves == 2 && kBoxRows == kChunk;   // one box per tile
     static_assert(kD * kElemBytes % 128 == 0, "rows must be whole 128-byte swizzle spans");
-    // Chunk k goes to stage k % NSTAGES and to consumer warp k % 4.  With
+    // Chunk k goes to stage k % NSTAGES and to warp k % 4.  With
     // NSTAGES a multiple of 4 every stage always belongs to the same warp, so
     // that warp waits on the stage's phases strictly one after another and a
     // parity wait can never match a phase two fills old.  Any other depth
@@ -70,7 +71,7 @@ struct Cfg {
 };
 
 // Ring depth (16-token chunks in flight per CTA): a multiple of the consumer
-// warp count, small enough that 4 CTAs fit an SM.
+// warp count, small enough that 5 CTAs fit an SM.
 #ifndef PA_DECODE_STAGES_16BIT
 #define PA_DECODE_STAGES_16BIT 4
 #endif
@@ -140,7 +141,7 @@ __device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t
     }
 }
 
-// One consumer warp's online-softmax state for up to 8 query heads (lane
+// One warp's online-softmax state for up to 8 query heads (lane
 // holds heads 2q, 2q+1) and its per-chunk step.
 template <pa_dtype KV, typename C>
 struct Consumer {
@@ -314,16 +315,12 @@ struct Consumer {
 // stage's barrier and issue the TMA boxes of the K and V tiles.  `pb_a` /
 // `pb_b` are the physical blocks of the chunk's first / second block (the
 // second only for 8-token blocks).  Returns false if a wait ran out.
-template <typename C, int BS, int NSTAGES>
-__device__ __forceinline__ bool issue_chunk(const DecodeArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                            uint64_t* full, uint64_t* empty, uint32_t ring, int k, int lane, int kvh,
-                                            int t0, int tok1, int pb_a, int pb_b, uint64_t policy) {
-    const int st = k % NSTAGES;
-    if (k >= NSTAGES) {
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(smem_addr(empty + st), ((k / NSTAGES) - 1) & 1);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-    }
+// Lane 0 arms stage st's full barrier with the chunk's byte count and
+// issues its K and V boxes (the stage must be free).
+template <typename C, int BS>
+__device__ __forceinline__ void issue_tiles(const DecodeArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                            uint64_t* full, uint32_t ring, int st, int lane, int kvh, int t0,
+                                            int tok1, int pb_a, int pb_b, uint64_t policy) {
     if (lane == 0) {
         const bool two = BS < kChunk && t0 + BS < tok1;   // second block holds valid tokens
         if (pb_a < 0 || pb_a >= a.num_blocks) {
@@ -358,8 +355,6 @@ __device__ __forceinline__ bool issue_chunk(const DecodeArgs& a, const CUtensorM
             }
         }
     }
-    __syncwarp();
-    return true;
 }
 
 // Block ids of an item's chunks, 32 at a time from one coalesced load.
@@ -392,17 +387,6 @@ struct BlockWindow {
     }
 };
 
-// After the last chunk: wait until every copy this CTA issued has landed
-// (they have, unless a wait ran out) before shared memory is reused or freed.
-template <int NSTAGES>
-__device__ __forceinline__ void drain_ring(const DecodeArgs& a, uint64_t* full, int issued, int lane) {
-    if (lane != 0) return;
-    for (int st = 0; st < NSTAGES && st < issued; ++st) {
-        const int fills = (issued - st + NSTAGES - 1) / NSTAGES;
-        if (!mbar_wait(smem_addr(full + st), (fills - 1) & 1)) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-    }
-}
-
 // Write one merged value: the final output, or this partition's partial.
 __device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, int d, int part, int n_parts,
                                              float val, float M, float L) {
@@ -419,7 +403,7 @@ __device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, i
 }
 
 // =====================================================================
-// Grid kernel: one CTA per (partition, KV head group, sequence)
+// The kernel: one CTA per (partition, KV head group, sequence)
 // =====================================================================
 
 template <pa_dtype KV, int BS, int NSTAGES>
@@ -427,21 +411,27 @@ struct GridCfg : Cfg<KV, BS, NSTAGES> {
     using B = Cfg<KV, BS, NSTAGES>;
     static constexpr int kMergeFloats = kConsumers * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
     static constexpr int kDataBytes = B::kRingBytes > kMergeFloats * 4 ? B::kRingBytes : kMergeFloats * 4;
-    static constexpr int kSmemBytes = 1024 + kDataBytes + 2 * NSTAGES * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + kDataBytes + NSTAGES * 8;   // + one full barrier per stage
 };
 
+// Every warp streams its own stages: stage s belongs to warp s % 4, which
+// issues its first NSTAGES / 4 chunks and, after consuming a chunk, has its
+// lane 0 issue the chunk NSTAGES ahead into the stage just freed.  With no
+// producer warp and no empty barriers a CTA is 4 warps, and the register
+// budget at 5 CTAs per SM is 96 per thread (no spills).  A separate producer
+// warp, tried first, left 72 registers (5 warps x 5 CTAs on 4 SM
+// sub-partitions) and spilled: long-context FP8 ran 220 us against 182.
 template <pa_dtype KV, int BS, int NSTAGES>
 __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_CTAS)
 decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const DecodeArgs a) {
     using C = GridCfg<KV, BS, NSTAGES>;
     constexpr bool kFp8 = KV == PA_FP8_E4M3;
+    constexpr int S = NSTAGES / kConsumers;   // stages per warp: warp w owns w, w + 4, ...
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
-    uint64_t* empty = full + NSTAGES;
-    int* abort_flag = reinterpret_cast<int*>(empty + NSTAGES);
     const uint32_t ring = smem_addr(smem);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -449,35 +439,21 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
     const int kvh = blockIdx.y / n_hg, hg = blockIdx.y - kvh * n_hg;
     const int part = blockIdx.x;
-
     const int h0 = kvh * a.group + hg * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
     const int32_t* bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
 
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
-    // The context length, the partition's first block ids and the query do
-    // not depend on one another: issue all three loads before waiting on
-    // any, so a CTA's first copy waits for one round trip less.  The ids are
-    // a guess (blocks from part * P / block_size, right without window starts
-    // when the partition share is P, and always for partition 0), used only
-    // once the real start confirms it.
     Consumer<KV, C> cs;
     cs.init(lane);
     cs.reset();
-    const bool spec = a.context_starts == nullptr;
-    int spec_ids = 0;
-    if (warp == kConsumers) {
-        if (lane == 0) {
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-        }
-        const int j = part * (a.partition_size / BS) + lane;
-        if (spec && j < a.max_blocks) spec_ids = __ldg(bt_row + j);
-    } else {
-        cs.template fetch_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
-                                  nh);
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
     }
+    cs.template fetch_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
+                              nh);
     const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
@@ -487,71 +463,65 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGES; ++i) {
-            mbar_init(smem_addr(full + i), 1);
-            mbar_init(smem_addr(empty + i), 1);
-        }
-        *abort_flag = 0;
+        for (int i = 0; i < NSTAGES; ++i) mbar_init(smem_addr(full + i), 1);
         fence_mbar_init();
     }
     __syncthreads();
+    const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
+    cs.convert_q(a.q_dtype == PA_BF16);
 
-    if (warp == kConsumers) {
-        // ------------------------------------------------------ producer
-        const uint64_t policy = l2_evict_first_policy();
-        BlockWindow win;
-        if (spec && tok0 == part * a.partition_size)
-            win.start_loaded(bt_row, tok0, tok1, BS, spec_ids);
-        else
-            win.start(bt_row, tok0, tok1, BS);
-        int issued = 0;
-        for (int c = 0; c < n_chunks; ++c) {
-            if (*reinterpret_cast<volatile int*>(abort_flag)) break;
-            const int t0 = tok0 + c * kChunk;
-            int pb_a, pb_b;
-            win.get(t0, BS, lane, pb_a, pb_b);
-            // an 8-token block wholly before a slid window may have been
-            // released: its rows (masked anyway) come from the chunk's second block
-            if (BS < kChunk && c == 0 && lead >= BS) pb_a = pb_b;
-            if (!issue_chunk<C, BS, NSTAGES>(a, &tmap_k, &tmap_v, full, empty, ring, c, lane, kvh, t0, tok1, pb_a,
-                                             pb_b, policy)) {
-                if (lane == 0) {
-                    atomicExch(abort_flag, 1);
-                    raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-                }
-                break;
-            }
+    const uint64_t policy = l2_evict_first_policy();
+    BlockWindow win;   // this warp's chunks, in increasing order
+    win.start(bt_row, tok0, tok1, BS);
+    auto issue = [&](int c, int st) {   // the whole warp: the block ids come by shuffle
+        const int t0 = tok0 + c * kChunk;
+        int pb_a, pb_b;
+        win.get(t0, BS, lane, pb_a, pb_b);
+        // an 8-token block wholly before a slid window may have been
+        // released: its rows (masked anyway) come from the chunk's second block
+        if (BS < kChunk && c == 0 && lead >= BS) pb_a = pb_b;
+        issue_tiles<C, BS>(a, &tmap_k, &tmap_v, full, ring, st, lane, kvh, t0, tok1, pb_a, pb_b, policy);
+    };
+    int issued = 0;   // this warp's chunks issued / consumed, in order
+    for (int s = 0; s < S; ++s) {
+        const int c = warp + kConsumers * s;
+        if (c < n_chunks) {
+            issue(c, warp + kConsumers * s);
             ++issued;
         }
-        drain_ring<NSTAGES>(a, full, issued, lane);
-    } else {
-        // ------------------------------------------------------ consumers
-        const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
-        cs.convert_q(a.q_dtype == PA_BF16);
-        for (int c = warp; c < n_chunks; c += kConsumers) {
-            const int st = c % NSTAGES;
-            const bool landed = mbar_wait(smem_addr(full + st), (c / NSTAGES) & 1);
-            if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
-                if (lane == 0) {
-                    atomicExch(abort_flag, 1);
-                    raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
-                }
-                break;
-            }
-            const uint32_t kb = ring + st * C::kStageBytes;
-            cs.chunk(kb, kb + C::kTileBytes, c == 0 ? lead : 0, min(kChunk, tok1 - (tok0 + c * kChunk)), sc);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(empty + st));
-        }
-        cs.finish();
     }
+    int k = 0;
+    for (int c = warp; c < n_chunks; c += kConsumers, ++k) {
+        const int st = warp + kConsumers * (k % S);
+        const bool landed = mbar_wait(smem_addr(full + st), (k / S) & 1);
+        if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
+            if (lane == 0) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
+            break;
+        }
+        const uint32_t kb = ring + st * C::kStageBytes;
+        cs.chunk(kb, kb + C::kTileBytes, c == 0 ? lead : 0, min(kChunk, tok1 - (tok0 + c * kChunk)), sc);
+        __syncwarp();
+        const int cn = c + kConsumers * S;
+        if (cn < n_chunks) {
+            if (lane == 0) fence_proxy_async_smem();   // the reads above before the copy's writes
+            issue(cn, st);
+            ++issued;
+        }
+    }
+    // copies still in flight (only after a wait ran out): let them land
+    // before the ring is reused
+    if (lane == 0)
+        for (int kk = k; kk < issued; ++kk)
+            if (!mbar_wait(smem_addr(full + warp + kConsumers * (kk % S)), (kk / S) & 1))
+                raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
+    cs.finish();
 
-    __syncthreads();  // every stage consumed (or drained): the ring becomes the merge buffer
+    __syncthreads();  // every stage consumed: the ring becomes the merge buffer
 
     float* mbuf = reinterpret_cast<float*>(smem);
     float* mm = mbuf + kConsumers * kHeadsPerCta * kMergeStride;
     float* ml = mm + kConsumers * kHeadsPerCta;
-    if (warp < kConsumers) {
+    {
         float* w0 = mbuf + (warp * kHeadsPerCta + 2 * cs.q4) * kMergeStride;
         float* w1 = w0 + kMergeStride;
 #pragma unroll
@@ -570,8 +540,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     __syncthreads();
 
-    if (threadIdx.x < kD) {
-        const int d = threadIdx.x;
+    {
+        const int d = threadIdx.x;   // 128 threads, one per element of head_dim
         const float vs = kFp8 ? a.v_scale : 1.f;
         for (int h = 0; h < nh; ++h) {
             float M = kNegInf;
@@ -655,12 +625,13 @@ pa_status launch(const DecodeArgs& a, cudaStream_t stream) {
     const int n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
     using C = GridCfg<KV, BS, NSTAGES>;
     auto kernel = decode_mma_kernel<KV, BS, NSTAGES>;
+    const int threads = kThreads;
     static std::once_flag once;   // once per instantiation
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [&] { err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes); });
     if (err != cudaSuccess) return PA_ERR_CUDA;
     dim3 grid(a.max_parts, a.num_kv_heads * n_hg, a.batch);
-    if (launch_pdl(kernel, grid, dim3(kThreads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(kernel, grid, dim3(threads), C::kSmemBytes, stream, mk, mv, a) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
 }
 
