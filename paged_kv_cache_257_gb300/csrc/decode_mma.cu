@@ -452,8 +452,16 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
+    // The query, the context length and the partition's first 32 block ids
+    // do not depend on one another: all are loaded before any is waited on.
+    // The ids are a guess (blocks from part * P / block_size: right without
+    // window starts when the partition share is P, and for partition 0),
+    // used only once the real partition start confirms it.
     cs.template fetch_q<true>(static_cast<const uint16_t*>(a.q) + (static_cast<int64_t>(seq) * a.num_q_heads + h0) * kD,
                               nh);
+    const bool spec = a.context_starts == nullptr;
+    const int spec_j = part * (a.partition_size / BS) + lane;
+    const int spec_ids = spec && spec_j < a.max_blocks ? __ldg(bt_row + spec_j) : 0;
     const SeqWindow sw = seq_window(a, seq, part == 0 && blockIdx.y == 0 && threadIdx.x == 0);
     const int n_parts = sw.n_parts;
     if (part >= n_parts) return;
@@ -472,7 +480,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     const uint64_t policy = l2_evict_first_policy();
     BlockWindow win;   // this warp's chunks, in increasing order
-    win.start(bt_row, tok0, tok1, BS);
+    if (spec && tok0 == part * a.partition_size)
+        win.start_loaded(bt_row, tok0, tok1, BS, spec_ids);
+    else
+        win.start(bt_row, tok0, tok1, BS);
     auto issue = [&](int c, int st) {   // the whole warp: the block ids come by shuffle
         const int t0 = tok0 + c * kChunk;
         int pb_a, pb_b;
