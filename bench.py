@@ -288,8 +288,8 @@ class GpuWorkload:
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h")
-NCU_TRAFFIC = {"7488f04de310508e": {"gqa_bf16": 283_142_144 + 3_683_072,
-                                    "longctx_fp8": 1_074_026_000 + 8_595_968}}
+NCU_TRAFFIC = {"a3bd468549c8b4a5": {"gqa_bf16": 283_139_840 + 3_213_312,
+                                    "longctx_fp8": 1_073_989_000 + 7_608_576}}
 
 
 def captured_traffic(workload):
