@@ -94,6 +94,16 @@ class NativeError(RuntimeError):
         super().__init__(f"{fn} failed: {self.status}")
 
 
+def load(path):
+    """A built copy of the library at ``path`` with every call's signature set."""
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     """The loaded library (built beforehand by ``paged_kv_cache_257_gb300.build``)."""
     global _lib
@@ -103,12 +113,7 @@ def lib():
                 raise RuntimeError(f"{LIB_PATH} is missing: build it first with "
                                    "paged_kv_cache_257_gb300.build.build() (nvcc, sm_103a); "
                                    "there is no fallback implementation")
-            L = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = load(LIB_PATH)
     return _lib
 
 

@@ -87,6 +87,31 @@ def build(force=False, jobs=None, extra_flags=(), verbose_ptxas=False):
     return LIB
 
 
+def build_variant(name, flags, recompile):
+    """A second copy of the library with ``flags`` added to the sources named
+    in ``recompile`` (file names in csrc/); every other object comes from the
+    main build.  Returns its path (``_build/<name>/libpagedattn.so``)."""
+    build()
+    out = os.path.join(BUILD, name)
+    os.makedirs(out, exist_ok=True)
+    objs = []
+    for src in sources():
+        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        if os.path.basename(src) in recompile:
+            obj = os.path.join(out, os.path.basename(src) + ".o")
+            cmd = [nvcc()] + ARCH + COMMON + list(flags) + ["-c", src, "-o", obj]
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+        objs.append(obj)
+    lib = os.path.join(out, "libpagedattn.so")
+    r = subprocess.run([nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", lib] + objs,
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv)
     print(LIB)

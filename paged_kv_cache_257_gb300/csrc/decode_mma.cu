@@ -315,6 +315,14 @@ struct Consumer {
 // stage's barrier and issue the TMA boxes of the K and V tiles.  `pb_a` /
 // `pb_b` are the physical blocks of the chunk's first / second block (the
 // second only for 8-token blocks).  Returns false if a wait ran out.
+// Test builds only (never the library's default build): arm each stage for
+// this many bytes more than its copies bring, so that no stage ever
+// completes and every wait runs into its time limit.  This is how the tests
+// check that a stalled copy ends in PA_DEVFLAG_TIMEOUT, not a hang.
+#ifndef PA_TEST_EXTRA_TX
+#define PA_TEST_EXTRA_TX 0
+#endif
+
 // Lane 0 arms stage st's full barrier with the chunk's byte count and
 // issues its K and V boxes (the stage must be free).
 template <typename C, int BS>
@@ -333,7 +341,7 @@ __device__ __forceinline__ void issue_tiles(const DecodeArgs& a, const CUtensorM
         }
         const int boxes = (two ? 2 : 1) * C::kHalves * 2;
         const uint32_t fb = smem_addr(full + st);
-        mbar_arrive_expect_tx(fb, boxes * C::kBoxBytes);
+        mbar_arrive_expect_tx(fb, boxes * C::kBoxBytes + PA_TEST_EXTRA_TX);
         const uint32_t kdst = ring + st * C::kStageBytes;
         const int ya = (pb_a * a.num_kv_heads + kvh) * BS + (t0 % BS);
         const int yb = (pb_b * a.num_kv_heads + kvh) * BS;
