@@ -67,7 +67,7 @@ struct Cfg {
     // that warp waits on the stage's phases strictly one after another and a
     // parity wait can never match a phase two fills old.  Any other depth
     // breaks that and must not be built.
-    static_assert(NSTAGES % kConsumers == 0, "each stage must belong to exactly one consumer warp");
+    static_assert(NSTAGES % kConsumers == 0, "each stage must belong to exactly one warp");
 };
 
 // Ring depth (16-token chunks in flight per CTA): a multiple of the consumer
@@ -311,10 +311,6 @@ struct Consumer {
     __device__ __forceinline__ int d_hi(int mt) const { return kFp8 ? 16 * mt + 2 * g + 1 : 16 * mt + g + 8; }
 };
 
-// Producer side of one chunk: wait for its stage to be free, then arm the
-// stage's barrier and issue the TMA boxes of the K and V tiles.  `pb_a` /
-// `pb_b` are the physical blocks of the chunk's first / second block (the
-// second only for 8-token blocks).  Returns false if a wait ran out.
 // Test builds only (never the library's default build): arm each stage for
 // this many bytes more than its copies bring, so that no stage ever
 // completes and every wait runs into its time limit.  This is how the tests
@@ -324,7 +320,9 @@ struct Consumer {
 #endif
 
 // Lane 0 arms stage st's full barrier with the chunk's byte count and
-// issues its K and V boxes (the stage must be free).
+// issues its K and V boxes (the stage must be free).  `pb_a` / `pb_b` are the
+// physical blocks of the chunk's first / second block (the second only for
+// 8-token blocks).
 template <typename C, int BS>
 __device__ __forceinline__ void issue_tiles(const DecodeArgs& a, const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                             uint64_t* full, uint32_t ring, int st, int lane, int kvh, int t0,
