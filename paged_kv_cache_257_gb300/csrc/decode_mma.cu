@@ -38,8 +38,8 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kChunk = 16;        // tokens per mma row tile
-constexpr int kConsumers = 4;     // warps per CTA, each consuming (and loading) its own stages
-constexpr int kThreads = kConsumers * 32;
+constexpr int kWarps = 4;         // warps per CTA, each loading and consuming its own stages
+constexpr int kThreads = kWarps * 32;
 constexpr int kMergeStride = kD + 4;  // floats per head row in merge buffers (bank spread)
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -67,10 +67,10 @@ struct Cfg {
     // that warp waits on the stage's phases strictly one after another and a
     // parity wait can never match a phase two fills old.  Any other depth
     // breaks that and must not be built.
-    static_assert(NSTAGES % kConsumers == 0, "each stage must belong to exactly one warp");
+    static_assert(NSTAGES % kWarps == 0, "each stage must belong to exactly one warp");
 };
 
-// Ring depth (16-token chunks in flight per CTA): a multiple of the consumer
+// Ring depth (16-token chunks in flight per CTA): a multiple of the
 // warp count, small enough that 5 CTAs fit an SM.
 #ifndef PA_DECODE_STAGES_16BIT
 #define PA_DECODE_STAGES_16BIT 4
@@ -144,7 +144,7 @@ __device__ __forceinline__ void pv_chunk(float (&o)[8][4], uint32_t vb, uint32_t
 // One warp's online-softmax state for up to 8 query heads (lane
 // holds heads 2q, 2q+1) and its per-chunk step.
 template <pa_dtype KV, typename C>
-struct Consumer {
+struct WarpState {
     static constexpr bool kFp8 = KV == PA_FP8_E4M3;
     static constexpr bool kBf16 = KV == PA_BF16;   // mma operand type: bf16, else f16
     float o[8][4];
@@ -415,7 +415,7 @@ __device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, i
 template <pa_dtype KV, int BS, int NSTAGES>
 struct GridCfg : Cfg<KV, BS, NSTAGES> {
     using B = Cfg<KV, BS, NSTAGES>;
-    static constexpr int kMergeFloats = kConsumers * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
+    static constexpr int kMergeFloats = kWarps * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
     static constexpr int kDataBytes = B::kRingBytes > kMergeFloats * 4 ? B::kRingBytes : kMergeFloats * 4;
     static constexpr int kSmemBytes = 1024 + kDataBytes + NSTAGES * 8;   // + one full barrier per stage
 };
@@ -433,7 +433,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                   const DecodeArgs a) {
     using C = GridCfg<KV, BS, NSTAGES>;
     constexpr bool kFp8 = KV == PA_FP8_E4M3;
-    constexpr int S = NSTAGES / kConsumers;   // stages per warp: warp w owns w, w + 4, ...
+    constexpr int S = NSTAGES / kWarps;   // stages per warp: warp w owns w, w + 4, ...
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -451,7 +451,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
-    Consumer<KV, C> cs;
+    WarpState<KV, C> cs;
     cs.init(lane);
     cs.reset();
     if (threadIdx.x == 0) {
@@ -501,15 +501,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     };
     int issued = 0;   // this warp's chunks issued / consumed, in order
     for (int s = 0; s < S; ++s) {
-        const int c = warp + kConsumers * s;
+        const int c = warp + kWarps * s;
         if (c < n_chunks) {
-            issue(c, warp + kConsumers * s);
+            issue(c, warp + kWarps * s);
             ++issued;
         }
     }
     int k = 0;
-    for (int c = warp; c < n_chunks; c += kConsumers, ++k) {
-        const int st = warp + kConsumers * (k % S);
+    for (int c = warp; c < n_chunks; c += kWarps, ++k) {
+        const int st = warp + kWarps * (k % S);
         const bool landed = mbar_wait(smem_addr(full + st), (k / S) & 1);
         if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
             if (lane == 0) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
@@ -518,7 +518,7 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         const uint32_t kb = ring + st * C::kStageBytes;
         cs.chunk(kb, kb + C::kTileBytes, c == 0 ? lead : 0, min(kChunk, tok1 - (tok0 + c * kChunk)), sc);
         __syncwarp();
-        const int cn = c + kConsumers * S;
+        const int cn = c + kWarps * S;
         if (cn < n_chunks) {
             if (lane == 0) fence_proxy_async_smem();   // the reads above before the copy's writes
             issue(cn, st);
@@ -529,15 +529,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     // before the ring is reused
     if (lane == 0)
         for (int kk = k; kk < issued; ++kk)
-            if (!mbar_wait(smem_addr(full + warp + kConsumers * (kk % S)), (kk / S) & 1))
+            if (!mbar_wait(smem_addr(full + warp + kWarps * (kk % S)), (kk / S) & 1))
                 raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
     cs.finish();
 
     __syncthreads();  // every stage consumed: the ring becomes the merge buffer
 
     float* mbuf = reinterpret_cast<float*>(smem);
-    float* mm = mbuf + kConsumers * kHeadsPerCta * kMergeStride;
-    float* ml = mm + kConsumers * kHeadsPerCta;
+    float* mm = mbuf + kWarps * kHeadsPerCta * kMergeStride;
+    float* ml = mm + kWarps * kHeadsPerCta;
     {
         float* w0 = mbuf + (warp * kHeadsPerCta + 2 * cs.q4) * kMergeStride;
         float* w1 = w0 + kMergeStride;
@@ -563,10 +563,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         for (int h = 0; h < nh; ++h) {
             float M = kNegInf;
 #pragma unroll
-            for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mm[w * kHeadsPerCta + h]);
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kHeadsPerCta + h]);
             float L = 0.f, acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumers; ++w) {
+            for (int w = 0; w < kWarps; ++w) {
                 const float mw = mm[w * kHeadsPerCta + h];
                 const float coef = mw == kNegInf ? 0.f : exp2_approx(mw - M);
                 L += coef * ml[w * kHeadsPerCta + h];
