@@ -288,8 +288,8 @@ class GpuWorkload:
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h")
-NCU_TRAFFIC = {"a3bd468549c8b4a5": {"gqa_bf16": 283_139_840 + 3_213_312,
-                                    "longctx_fp8": 1_073_989_000 + 7_608_576}}
+NCU_TRAFFIC = {"0cf96aaed47e2739": {"gqa_bf16": 283_139_840 + 3_437_824,
+                                    "longctx_fp8": 1_074_041_000 + 7_970_816}}
 
 
 def captured_traffic(workload):
