@@ -5,8 +5,11 @@ of the step's new tokens (slot scatter kernel) and single-query paged decode
 attention (decode kernel + split-context merge kernel).  Inputs are seeded
 and synthetic; the caches are built through the library before timing.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--partition P]
+                    [--window W] [--block-size 8|16|32] [--no-cpu-baseline]
     python bench.py --impl reference ...     # the oracle on the host cores
+
+NAME is gqa_bf16 (the default), mha_f16, prefix_bf16 or longctx_fp8.
 
 Prints one JSON line.  ``value`` is decode tokens/s (batch x steps / time)
 with every input resident in HBM; ``e2e`` is the same metric through the
