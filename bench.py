@@ -640,7 +640,9 @@ def main():
     init_distributed(world)
     import torch
     from paged_kv_cache_257_gb300 import build
-    build.build()
+    if rank == 0:          # one build for all ranks: they share the source tree
+        build.build()
+    barrier()
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
     from synth import workloads as wl

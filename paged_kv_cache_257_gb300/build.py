@@ -50,13 +50,14 @@ def _compile(src, extra, verbose_ptxas):
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     if not _stale(obj, [src] + _headers()):
         return obj, ""
-    cmd = [nvcc()] + ARCH + COMMON + list(extra) + ["-c", src, "-o", obj + ".tmp"]
+    tmp = obj + f".tmp{os.getpid()}"   # a name of its own: concurrent builds never share a file
+    cmd = [nvcc()] + ARCH + COMMON + list(extra) + ["-c", src, "-o", tmp]
     if verbose_ptxas and src.endswith(".cu"):
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
-    os.replace(obj + ".tmp", obj)
+    os.replace(tmp, obj)
     return obj, r.stderr
 
 
