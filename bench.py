@@ -290,9 +290,10 @@ class GpuWorkload:
 # files below, concatenated); after any change to them traffic is reported as
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
-                   "paged_kv_cache_257_gb300/csrc/decode.h")
-NCU_TRAFFIC = {"0cf96aaed47e2739": {"gqa_bf16": 283_139_840 + 3_437_824,
-                                    "longctx_fp8": 1_074_041_000 + 7_970_816}}
+                   "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
+                   "paged_kv_cache_257_gb300/csrc/window.cuh")
+NCU_TRAFFIC = {"e009e76f891c1758": {"gqa_bf16": 283_159_040 + 3_432_704,
+                                    "longctx_fp8": 1_074_032_896 + 7_943_680}}
 
 
 def captured_traffic(workload):

@@ -40,6 +40,7 @@ constexpr int kD = 128;
 constexpr int kChunk = 16;        // tokens per mma row tile
 constexpr int kWarps = 4;         // warps per CTA, each loading and consuming its own stages
 constexpr int kThreads = kWarps * 32;
+constexpr int kDynTailChunks = 16;   // chunks at the end of an item shared out by a counter
 constexpr int kMergeStride = kD + 4;  // floats per head row in merge buffers (bank spread)
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -476,9 +477,15 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     const int lead = sw.lead(part);   // positions of chunk 0 before the window
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
 
+    // the first chunk handed out by the counter below (a multiple of 4, past
+    // the prologue's chunks)
+    constexpr bool kClaims = S == 1;
+    const int t_dyn = kClaims ? max(NSTAGES, (n_chunks - kDynTailChunks) & ~(kWarps - 1)) : n_chunks;
+    __shared__ int next_chunk;   // the next chunk no warp has taken yet
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGES; ++i) mbar_init(smem_addr(full + i), 1);
         fence_mbar_init();
+        next_chunk = t_dyn;
     }
     __syncthreads();
     const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
@@ -499,6 +506,22 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (BS < kChunk && c == 0 && lead >= BS) pb_a = pb_b;
         issue_tiles<C, BS>(a, &tmap_k, &tmap_v, full, ring, st, lane, kvh, t0, tok1, pb_a, pb_b, policy);
     };
+    // Chunk schedule.  Chunks below t_dyn go to the warps in a fixed
+    // pattern: warp w takes w, w + 4, w + 8, ...  With one stage per warp
+    // (16-bit caches) the last kDynTailChunks chunks are handed out in order
+    // from a CTA-wide counter instead: a warp that has consumed a chunk takes
+    // the next untaken one into the stage it just freed.  Warps whose copies
+    // landed sooner take more of the tail, so the CTA's warps finish within
+    // about one copy of one another; with the fixed pattern alone they ended
+    // a median 2.7 us (up to 11 us) apart on the Llama-3-8B ragged batch,
+    // which the tail counter makes 3% faster.  The counter stays out of the
+    // rest of the loop: a claim per chunk (a shared-memory atomic and a
+    // shuffle) made batches whose shared prefix is read from L2 4% slower.
+    // FP8 warps (two copies in flight each) finish close together and keep
+    // the fixed pattern to the end.  Either way a warp's chunks come in
+    // increasing order and its stages are used round robin: the k-th chunk
+    // it consumes sits in stage warp + 4 (k % S) with phase (k / S) & 1.
+    static_assert(!kClaims || S == 1, "claimed chunks are consumed in issue order only with one stage per warp");
     int issued = 0;   // this warp's chunks issued / consumed, in order
     for (int s = 0; s < S; ++s) {
         const int c = warp + kWarps * s;
@@ -508,22 +531,28 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         }
     }
     int k = 0;
-    for (int c = warp; c < n_chunks; c += kWarps, ++k) {
+    for (int c = warp; c < n_chunks; ++k) {
         const int st = warp + kWarps * (k % S);
         const bool landed = mbar_wait(smem_addr(full + st), (k / S) & 1);
         if (!__all_sync(0xffffffffu, landed)) {   // warp-uniform decision
             if (lane == 0) raise_flag(a.status, PA_DEVFLAG_TIMEOUT);
             break;
         }
+        int cn = c + kWarps * S;   // the chunk to bring into this stage next
+        const bool claim = kClaims && cn >= t_dyn;   // warp-uniform
+        if (claim && lane == 0) cn = atomicAdd(&next_chunk, 1);   // claimed now: its latency overlaps the math
         const uint32_t kb = ring + st * C::kStageBytes;
         cs.chunk(kb, kb + C::kTileBytes, c == 0 ? lead : 0, min(kChunk, tok1 - (tok0 + c * kChunk)), sc);
         __syncwarp();
-        const int cn = c + kWarps * S;
+        if (claim) cn = __shfl_sync(0xffffffffu, cn, 0);
         if (cn < n_chunks) {
             if (lane == 0) fence_proxy_async_smem();   // the reads above before the copy's writes
             issue(cn, st);
             ++issued;
         }
+        // next to consume: with one stage per warp, the chunk just issued
+        // (n_chunks or more: none); else the fixed pattern's next
+        c = kClaims ? cn : c + kWarps;
     }
     // copies still in flight (only after a wait ran out): let them land
     // before the ring is reused
@@ -560,20 +589,29 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     {
         const int d = threadIdx.x;   // 128 threads, one per element of head_dim
         const float vs = kFp8 ? a.v_scale : 1.f;
-        for (int h = 0; h < nh; ++h) {
-            float M = kNegInf;
+        // four heads at a time, unrolled (every warp wrote all kHeadsPerCta
+        // heads; only the group's nh are stored).  Measured against a plain
+        // loop over the nh heads: the same on most batches, 6% faster on a
+        // batch whose shared prefix is read from L2.
+        static_assert(kHeadsPerCta % 4 == 0, "heads are merged four at a time");
+        for (int h4 = 0; h4 < nh; h4 += 4) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kHeadsPerCta + h]);
-            float L = 0.f, acc = 0.f;
+            for (int j = 0; j < 4; ++j) {
+                const int h = h4 + j;
+                float M = kNegInf;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = mm[w * kHeadsPerCta + h];
-                const float coef = mw == kNegInf ? 0.f : exp2_approx(mw - M);
-                L += coef * ml[w * kHeadsPerCta + h];
-                acc += coef * mbuf[(w * kHeadsPerCta + h) * kMergeStride + d];
+                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kHeadsPerCta + h]);
+                float L = 0.f, acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float mw = mm[w * kHeadsPerCta + h];
+                    const float coef = mw == kNegInf ? 0.f : exp2_approx(mw - M);
+                    L += coef * ml[w * kHeadsPerCta + h];
+                    acc += coef * mbuf[(w * kHeadsPerCta + h) * kMergeStride + d];
+                }
+                const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h0 + h;
+                if (h < nh) store_result(a, row, d, part, n_parts, L > 0.f ? acc * vs / L : 0.f, M, L);
             }
-            const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h0 + h;
-            store_result(a, row, d, part, n_parts, L > 0.f ? acc * vs / L : 0.f, M, L);
         }
     }
     if (n_parts > 1 && a.fused_merge) {
