@@ -416,7 +416,10 @@ __device__ __forceinline__ void store_result(const DecodeArgs& a, int64_t row, i
 template <pa_dtype KV, int BS, int NSTAGES>
 struct GridCfg : Cfg<KV, BS, NSTAGES> {
     using B = Cfg<KV, BS, NSTAGES>;
-    static constexpr int kMergeFloats = kWarps * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta);
+    // merge buffers: the warps' o rows, their (m, l) per head, the merged
+    // (M, L) per head and a staging area for a partial's bulk store
+    static constexpr int kMergeFloats =
+        kWarps * (kHeadsPerCta * kMergeStride + 2 * kHeadsPerCta) + 2 * kHeadsPerCta + kHeadsPerCta * kD;
     static constexpr int kDataBytes = B::kRingBytes > kMergeFloats * 4 ? B::kRingBytes : kMergeFloats * 4;
     static constexpr int kSmemBytes = 1024 + kDataBytes + NSTAGES * 8;   // + one full barrier per stage
 };
@@ -565,8 +568,10 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     __syncthreads();  // every stage consumed: the ring becomes the merge buffer
 
     float* mbuf = reinterpret_cast<float*>(smem);
-    float* mm = mbuf + kWarps * kHeadsPerCta * kMergeStride;
-    float* ml = mm + kWarps * kHeadsPerCta;
+    float* mm = mbuf + kWarps * kHeadsPerCta * kMergeStride;   // (warp, head): max, then the warp's weight
+    float* ml = mm + kWarps * kHeadsPerCta;                    // (warp, head): row sum
+    float* hml = ml + kWarps * kHeadsPerCta;                   // head: merged (M, L)
+    float* stage = hml + 2 * kHeadsPerCta;                     // [head][kD]: a partial for its bulk store
     {
         float* w0 = mbuf + (warp * kHeadsPerCta + 2 * cs.q4) * kMergeStride;
         float* w1 = w0 + kMergeStride;
@@ -586,9 +591,36 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     __syncthreads();
 
+    const float vs = kFp8 ? a.v_scale : 1.f;
+    // Warp 0 weighs the warps' partial states once, lane = w * 8 + h:
+    //     M_h = max_w m_wh,  L_h = sum_w 2^(m_wh - M_h) l_wh,
+    //     weight_wh = 2^(m_wh - M_h) vs / L_h (0 for an empty head).
+    // Every thread then only sums weighted o rows (each thread redoing the
+    // exponentials took about twice as long).
+    static_assert(kWarps * kHeadsPerCta == 32, "one lane of warp 0 per (warp, head)");
+    if (warp == 0) {
+        const float m = mm[lane];
+        float M = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+        const float coef = m == kNegInf ? 0.f : exp2_approx(m - M);
+        float L = coef * ml[lane];
+        L += __shfl_xor_sync(0xffffffffu, L, 8);
+        L += __shfl_xor_sync(0xffffffffu, L, 16);
+        mm[lane] = L > 0.f ? coef * vs / L : 0.f;   // each lane rewrites only its own entry
+        if (lane < kHeadsPerCta) {
+            hml[2 * lane] = M;
+            hml[2 * lane + 1] = L;
+        }
+    }
+    __syncthreads();
+
+    // A split call's partials go out as one bulk copy per head when the merge
+    // kernel reads them (its launch orders them), so that a CTA does not wait
+    // on stores to a busy memory system; the fused merge's ticket needs its
+    // partials visible first and keeps plain stores.
+    const bool bulk = n_parts > 1 && !a.fused_merge;
     {
         const int d = threadIdx.x;   // 128 threads, one per element of head_dim
-        const float vs = kFp8 ? a.v_scale : 1.f;
         // four heads at a time, unrolled (every warp wrote all kHeadsPerCta
         // heads; only the group's nh are stored).  Measured against a plain
         // loop over the nh heads: the same on most batches, 6% faster on a
@@ -598,20 +630,33 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int h = h4 + j;
-                float M = kNegInf;
+                float acc = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mm[w * kHeadsPerCta + h]);
-                float L = 0.f, acc = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float mw = mm[w * kHeadsPerCta + h];
-                    const float coef = mw == kNegInf ? 0.f : exp2_approx(mw - M);
-                    L += coef * ml[w * kHeadsPerCta + h];
-                    acc += coef * mbuf[(w * kHeadsPerCta + h) * kMergeStride + d];
-                }
+                for (int w = 0; w < kWarps; ++w)
+                    acc = fmaf(mm[w * kHeadsPerCta + h], mbuf[(w * kHeadsPerCta + h) * kMergeStride + d], acc);
                 const int64_t row = static_cast<int64_t>(seq) * a.num_q_heads + h0 + h;
-                if (h < nh) store_result(a, row, d, part, n_parts, L > 0.f ? acc * vs / L : 0.f, M, L);
+                if (h < nh) {
+                    if (bulk)
+                        stage[h * kD + d] = acc;
+                    else
+                        store_result(a, row, d, part, n_parts, acc, hml[2 * h], hml[2 * h + 1]);
+                }
             }
+        }
+    }
+    if (bulk) {
+        const int64_t row0 = static_cast<int64_t>(seq) * a.num_q_heads + h0;
+        if (threadIdx.x < nh) {   // (M, L) of one head: 8 bytes
+            const int64_t pi = (row0 + threadIdx.x) * a.max_parts + part;
+            reinterpret_cast<float2*>(a.part_ml)[pi] = make_float2(hml[2 * threadIdx.x], hml[2 * threadIdx.x + 1]);
+        }
+        fence_proxy_async_smem();   // the staged rows, written by every thread, before the copies read them
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int h = 0; h < nh; ++h)
+                bulk_store(a.part_o + ((row0 + h) * a.max_parts + part) * kD, smem_addr(stage + h * kD), kD * 4);
+            bulk_commit();
+            bulk_wait_read();   // shared memory stays until the copies have read it
         }
     }
     if (n_parts > 1 && a.fused_merge) {
