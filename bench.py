@@ -292,8 +292,8 @@ class GpuWorkload:
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
-NCU_TRAFFIC = {"e009e76f891c1758": {"gqa_bf16": 283_159_040 + 3_432_704,
-                                    "longctx_fp8": 1_074_032_896 + 7_943_680}}
+NCU_TRAFFIC = {"78c55ec0130ecd5a": {"gqa_bf16": 283_155_712 + 3_357_184,
+                                    "longctx_fp8": 1_074_031_104 + 7_497_472}}
 
 
 def captured_traffic(workload):
@@ -426,6 +426,46 @@ def _stats_us(ms):
     return {"mean": statistics.mean(ms) * 1e3, "median": statistics.median(ms) * 1e3, "min": min(ms) * 1e3}
 
 
+class E2EBuffers:
+    """Pinned host and device buffers of the end-to-end loop.  Every input
+    of a step sits in one pinned staging buffer (256-byte aligned pieces), so
+    a step uploads with one copy; typed views name the pieces on the device."""
+
+    def __init__(self, wk):
+        torch = wk.torch
+        host = {"q": wk.q.cpu().pin_memory(), "bt": wk.block_tables.cpu().pin_memory(),
+                "ctx": wk.context_lens.cpu().pin_memory()}
+        if wk.context_starts is not None:
+            host["starts"] = wk.context_starts.cpu().pin_memory()
+        if wk.new_k is not None:
+            host.update(k=wk.new_k.cpu().pin_memory(), v=wk.new_v.cpu().pin_memory(),
+                        slots=wk.new_slots.cpu().pin_memory())
+        self.out_host = [torch.empty(wk.out.shape, dtype=wk.out.dtype).pin_memory() for _ in range(2)]
+        self.outs = [torch.empty_like(wk.out) for _ in range(2)]
+        offs, size = {}, 0
+        for k, v in host.items():
+            offs[k] = size
+            size += (v.numel() * v.element_size() + 255) // 256 * 256
+        self.stage = torch.empty(size, dtype=torch.uint8).pin_memory()
+        for k, v in host.items():
+            n = v.numel() * v.element_size()
+            self.stage[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
+        self.bufs = [torch.empty(size, dtype=torch.uint8, device=wk.device) for _ in range(2)]
+        self.dev = [{k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                     for k, v in host.items()} for buf in self.bufs]
+        self.h2d = sum(v.numel() * v.element_size() for v in host.values())
+        self.d2h = self.out_host[0].numel() * self.out_host[0].element_size()
+
+
+def e2e_compute(wk, d, out, r, part):
+    """One step's device work through the public API on the current stream."""
+    kc, vc = wk.pools[r % len(wk.pools)]
+    if "k" in d:
+        wk.pa.kv_append(wk.desc, d["k"], d["v"], d["slots"], kc, vc)
+    wk.pa.decode_attention(wk.desc, d["q"], kc, vc, d["bt"], d["ctx"], wk.w.scale, partition=part,
+                           workspace=wk.workspace, out=out, context_starts=d.get("starts"))
+
+
 def time_e2e(wk, steps, warmup):
     """The public API from pinned host buffers, as a serving loop drives it:
     every step uploads its inputs and downloads its output.  The uploads and
@@ -433,35 +473,8 @@ def time_e2e(wk, steps, warmup):
     step's inputs and the previous step's output move while this step
     computes; a buffer is reused only after the step two back has finished
     with it.  The timed region ends when the last output is in host memory."""
-    torch, pa = wk.torch, wk.pa
-    host = {"q": wk.q.cpu().pin_memory(), "bt": wk.block_tables.cpu().pin_memory(),
-            "ctx": wk.context_lens.cpu().pin_memory()}
-    if wk.context_starts is not None:
-        host["starts"] = wk.context_starts.cpu().pin_memory()
-    if wk.new_k is not None:
-        host.update(k=wk.new_k.cpu().pin_memory(), v=wk.new_v.cpu().pin_memory(),
-                    slots=wk.new_slots.cpu().pin_memory())
-    out_host = [torch.empty(wk.out.shape, dtype=wk.out.dtype).pin_memory() for _ in range(2)]
-    outs = [torch.empty_like(wk.out) for _ in range(2)]
-    # every input of a step in one pinned staging buffer (256-byte aligned
-    # pieces), so a step uploads with one copy; typed views on each side
-    offs, size = {}, 0
-    for k, v in host.items():
-        offs[k] = size
-        size += (v.numel() * v.element_size() + 255) // 256 * 256
-    stage = torch.empty(size, dtype=torch.uint8).pin_memory()
-    for k, v in host.items():
-        n = v.numel() * v.element_size()
-        stage[offs[k]:offs[k] + n].copy_(v.contiguous().view(-1).view(torch.uint8))
-    bufs = [torch.empty(size, dtype=torch.uint8, device=wk.device) for _ in range(2)]
-
-    def views(buf):
-        return {k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
-                for k, v in host.items()}
-
-    dev = [views(buf) for buf in bufs]
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host[0].numel() * out_host[0].element_size()
+    torch = wk.torch
+    eb = E2EBuffers(wk)
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     computed = [torch.cuda.Event() for _ in range(2)]     # step done with dev[b], outs[b] written
@@ -475,21 +488,16 @@ def time_e2e(wk, steps, warmup):
         b = r % 2
         with torch.cuda.stream(up):
             up.wait_event(computed[b])
-            bufs[b].copy_(stage, non_blocking=True)
+            eb.bufs[b].copy_(eb.stage, non_blocking=True)
             uploaded[b].record(up)
         comp.wait_event(uploaded[b])
         comp.wait_event(downloaded[b])
-        kc, vc = wk.pools[r % len(wk.pools)]
-        d = dev[b]
-        if "k" in d:
-            pa.kv_append(wk.desc, d["k"], d["v"], d["slots"], kc, vc)
         part = wk.plan_partition() if wk.plan else wk.partition   # host work of a serving step
-        pa.decode_attention(wk.desc, d["q"], kc, vc, d["bt"], d["ctx"], wk.w.scale,
-                            partition=part, workspace=wk.workspace, out=outs[b], context_starts=d.get("starts"))
+        e2e_compute(wk, eb.dev[b], eb.outs[b], r, part)
         computed[b].record(comp)
         with torch.cuda.stream(down):
             down.wait_event(computed[b])
-            out_host[b].copy_(outs[b], non_blocking=True)
+            eb.out_host[b].copy_(eb.outs[b], non_blocking=True)
             downloaded[b].record(down)
 
     for i in range(warmup):
@@ -505,7 +513,68 @@ def time_e2e(wk, steps, warmup):
     comp.wait_event(downloaded[(warmup + steps - 1) % 2])
     end.record(comp)
     torch.cuda.synchronize()
-    return start.elapsed_time(end), h2d, d2h
+    return start.elapsed_time(end), eb.h2d, eb.d2h
+
+
+def time_e2e_graph(wk, steps, warmup):
+    """The same serving loop with each step replayed from a CUDA graph, the
+    way decode steps of a fixed batch shape are usually launched.
+
+    Graph i (buffer set b = i % 2, cache replica i % R) computes on dev[b]
+    (uploaded by the graph before it), uploads the next step's inputs into
+    dev[1 - b] and downloads the previous step's output from outs[1 - b]; the
+    copies are branches of the graph that run beside the kernels.  Graphs
+    replay in stream order, so each buffer's writer has finished before its
+    reader starts.  The partition size is planned once on the host: the
+    batch's lengths do not change between these steps (a serving loop keeps
+    one graph per batch shape and partition size).  Returns (ms, h2d, d2h) of
+    the timed steps, including the first upload and the last download."""
+    torch = wk.torch
+    eb = E2EBuffers(wk)
+    part = wk.plan_partition() if wk.plan else wk.partition
+    n_graphs = 2 * len(wk.pools) // math.gcd(2, len(wk.pools))
+    side = torch.cuda.Stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    for buf in eb.bufs:                                 # valid inputs in both sets before any compute
+        buf.copy_(eb.stage)
+    with torch.cuda.stream(side):                       # warm-up before capture
+        for i in range(n_graphs):
+            e2e_compute(wk, eb.dev[i % 2], eb.outs[i % 2], i, part)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(n_graphs):
+        b = i % 2
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            cs = torch.cuda.current_stream()
+            up.wait_stream(cs)
+            down.wait_stream(cs)
+            with torch.cuda.stream(up):
+                eb.bufs[1 - b].copy_(eb.stage, non_blocking=True)
+            with torch.cuda.stream(down):
+                eb.out_host[1 - b].copy_(eb.outs[1 - b], non_blocking=True)
+            e2e_compute(wk, eb.dev[b], eb.outs[b], i, part)
+            cs.wait_stream(up)
+            cs.wait_stream(down)
+        graphs.append(g)
+    comp = torch.cuda.current_stream()
+
+    def run(n):
+        eb.bufs[0].copy_(eb.stage, non_blocking=True)
+        for i in range(n):
+            graphs[i % n_graphs].replay()
+        eb.out_host[(n - 1) % 2].copy_(eb.outs[(n - 1) % 2], non_blocking=True)
+
+    run(max(warmup, n_graphs))
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(comp)
+    run(steps)
+    end.record(comp)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end), eb.h2d, eb.d2h
 
 
 # -------------------------------------------------------------- oracle arm
@@ -655,9 +724,15 @@ def main():
     with ClockSampler(local) as clk:
         total_ms, dec_ms, app_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
     no_flush_ms = time_decode_no_flush(wk, args.steps)
-    e2e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
+    eager_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
+    try:
+        e2e_ms, h2d, d2h = time_e2e_graph(wk, args.steps, args.warmup)
+        e2e_mode = "graph"
+    except RuntimeError as e:                            # capture refused: the eager loop's number stands
+        e2e_ms, e2e_mode = eager_ms, f"eager (graph capture failed: {str(e).splitlines()[0][:120]})"
     value, total_ms = job_rate(w.batch, args.steps, world, total_ms)
     e2e_value, e2e_ms = job_rate(w.batch, args.steps, world, e2e_ms)
+    eager_value, eager_ms = job_rate(w.batch, args.steps, world, eager_ms)
     dec_avg_s = statistics.mean(dec_ms) / 1e3
     peak, peak_src = measured_peak()
     achieved = wk.kv_bytes / dec_avg_s / 1e9
@@ -683,7 +758,9 @@ def main():
                      "traffic": captured_traffic(args.workload), "traffic_of": "one decode_mma_kernel launch (ncu)",
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes,
                      "nominal_peak_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "launch": e2e_mode, "eager_value": eager_value,
+                "eager_note": "the same loop launching each call from Python, planning the partition every step"},
         "gpu_launches": launches,
         "clocks": dict(clk.summary(), window=f"{args.clock_probe_s:.1f} s of the same steps + the timed steps"),
     }
