@@ -747,6 +747,8 @@ def main():
                    "partition_size": wk.resolved_partition, "append_tokens": w.append_tokens,
                    "l2": f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)",
                    "parallelism": f"replicas x{world}",
+                   "decode_schedule": "deterministic" if wk.pa.decode_deterministic() else
+                   "balanced tail (the library's default; reproducible to bf16 rounding)",
                    **({"window": args.window} if args.window > 0 else {})},
         "kv_tokens_per_s": wk.kv_tokens * world / step_s,
         "kv_gbs": wk.kv_bytes * world / step_s / 1e9,

@@ -219,7 +219,11 @@ size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32
  * q_dtype PA_F32, PA_F16 or PA_BF16 (PA_F16/PA_BF16 queries with an FP8
  * cache must lie within the float16 range).  Tensor cores serve 16-bit and
  * FP8 caches with head_dim 128 and 16-bit queries; other cases run on CUDA
- * cores. */
+ * cores.  Results are reproducible bit for bit only in the deterministic
+ * schedule (pa_set_decode_deterministic).
+ * Errors: PA_ERR_INVALID (bad sizes or scale, null or misaligned pointers, a
+ * workspace smaller than needed), PA_ERR_UNSUPPORTED (dtype pair, grid
+ * limits), PA_ERR_CUDA (a launch failed). */
 pa_status pa_decode_attention(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
                               int32_t num_q_heads, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -270,12 +274,28 @@ pa_status pa_decode_attention_window(const pa_cache_desc* cache, const void* q, 
  *     stream before the kernels.  Calls whose kernels overlap on the GPU
  *     (other streams, other host threads) race on the array: serialise them. */
 #define PA_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
 pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, const void* q, pa_dtype q_dtype,
                                       int32_t num_q_heads, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
                                       const int32_t* context_lens, int32_t batch, float scale,
                                       int32_t partition_size, void* out, pa_dtype out_dtype,
                                       int32_t* device_status, void* stream);
+
+/* Chunk schedule of the tensor-core decode kernel, for every later decode
+ * call of the process.  The pages have no counterpart: it is a property of
+ * this kernel.  Default (0): with 16-bit caches the last 16 chunks of a work
+ * item go to whichever of the CTA's warps is free, which balances the warps
+ * (Llama-3-8B ragged batch about 3% faster).  A warp's softmax reference and
+ * summation order then depend on timing, so two runs on the same inputs can
+ * differ at the level of bf16 rounding of the probabilities (well inside the
+ * documented tolerance, but not bit for bit).  1: every chunk goes to a
+ * fixed warp; results are bit-reproducible.  FP8 caches and the CUDA-core
+ * kernel always use fixed schedules.  Takes effect for calls made after it
+ * returns (a process-wide setting; no synchronisation with calls in flight).
+ * pa_get_decode_deterministic returns the current setting. */
+void pa_set_decode_deterministic(int32_t on);
+int32_t pa_get_decode_deterministic(void);
 
 /* Wait for `stream`, copy the device status word to *flags_out (may be
  * NULL) and, if `reset` is non-zero, zero it.  Returns PA_ERR_DEVICE_FLAG

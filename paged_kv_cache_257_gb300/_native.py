@@ -58,6 +58,8 @@ SIGNATURES = {
                                                    c_void_p, c_int32, c_void_p, c_int32, c_float, c_int32, c_void_p,
                                                    ctypes.c_int, c_void_p, c_void_p]),
     "pa_read_device_status": (ctypes.c_int, [c_void_p, P_int32, c_int32, c_void_p]),
+    "pa_set_decode_deterministic": (None, [c_int32]),
+    "pa_get_decode_deterministic": (c_int32, []),
     "pa_alloc_create": (ctypes.c_int, [c_int32, c_uint64, ctypes.POINTER(c_void_p)]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_alloc_num_blocks": (c_int32, [c_void_p]),

@@ -228,6 +228,22 @@ def decode_attention_noalloc(desc, q, k_cache, v_cache, block_tables, context_le
     return out
 
 
+def set_decode_deterministic(on):
+    """``pa_set_decode_deterministic``: True gives bit-reproducible decode
+    results (every chunk on a fixed warp); False (the default) lets the
+    warps of a CTA share out an item's last chunks, which is faster and
+    reproducible to bf16 rounding of the probabilities only.  Process-wide;
+    returns the previous setting."""
+    prev = bool(lib().pa_get_decode_deterministic())
+    lib().pa_set_decode_deterministic(1 if on else 0)
+    return prev
+
+
+def decode_deterministic():
+    """The current ``pa_set_decode_deterministic`` setting."""
+    return bool(lib().pa_get_decode_deterministic())
+
+
 def new_workspace(nbytes, device="cuda"):
     """A zero-filled decode workspace (the library keeps its counters zero between calls)."""
     return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)

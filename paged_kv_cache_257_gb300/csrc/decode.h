@@ -22,6 +22,7 @@ struct DecodeArgs {
     float* part_ml;               // [batch][num_q_heads][max_parts][2]: (max, sum) in log2 units
     int32_t* tickets;             // [batch][num_kv_heads * head groups], zero between calls
     int32_t fused_merge;          // 1: the last CTA of a group merges; 0: the merge kernel does
+    int32_t balanced_tail;        // 1: the tensor-core kernel shares an item's last chunks among its warps
     int32_t* status;              // device status word or null
     int32_t batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks;
     int32_t group;                // num_q_heads / num_kv_heads

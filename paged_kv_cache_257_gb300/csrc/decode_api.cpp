@@ -1,6 +1,7 @@
 // Entry points of decode attention: argument checks, partition choice,
 // workspace layout and kernel dispatch.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -11,6 +12,8 @@ namespace pa {
 namespace {
 
 constexpr int kMaxParts = 32768;
+
+std::atomic<int32_t> g_deterministic{0};   // pa_set_decode_deterministic
 
 // Workspace layout of a split call: merge tickets, partial outputs and
 // partial (max, sum) pairs.  An unsplit call needs none.
@@ -193,6 +196,7 @@ extern "C" pa_status pa_decode_attention_window(const pa_cache_desc* cache, cons
     a.part_o = split ? reinterpret_cast<float*>(ws + wl.tickets_bytes) : nullptr;
     a.part_ml = split ? reinterpret_cast<float*>(ws + wl.tickets_bytes + wl.part_o_bytes) : nullptr;
     a.fused_merge = parts <= kFusedMergeMaxParts ? 1 : 0;
+    a.balanced_tail = g_deterministic.load(std::memory_order_relaxed) ? 0 : 1;
     a.status = device_status;
     a.batch = batch;
     a.num_q_heads = num_q_heads;
@@ -227,3 +231,7 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
                                       max_blocks_per_seq, context_lens, nullptr, batch, scale, partition_size,
                                       workspace, workspace_bytes, out, out_dtype, device_status, stream);
 }
+
+extern "C" void pa_set_decode_deterministic(int32_t on) { g_deterministic.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+extern "C" int32_t pa_get_decode_deterministic(void) { return g_deterministic.load(std::memory_order_relaxed); }

@@ -483,7 +483,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     // the first chunk handed out by the counter below (a multiple of 4, past
     // the prologue's chunks)
     constexpr bool kClaims = S == 1;
-    const int t_dyn = kClaims ? max(NSTAGES, (n_chunks - kDynTailChunks) & ~(kWarps - 1)) : n_chunks;
+    const int t_dyn = kClaims && a.balanced_tail ? max(NSTAGES, (n_chunks - kDynTailChunks) & ~(kWarps - 1))
+                                                 : n_chunks + kWarps * S;   // past every chunk: no claims
     __shared__ int next_chunk;   // the next chunk no warp has taken yet
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSTAGES; ++i) mbar_init(smem_addr(full + i), 1);

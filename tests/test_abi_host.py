@@ -36,6 +36,17 @@ def test_binding_declares_every_symbol(pa):
     assert set(_declared()) == set(_native.SIGNATURES)
 
 
+def test_decode_deterministic_setting_round_trips(pa):
+    prev = pa.decode_deterministic()
+    try:
+        assert pa.set_decode_deterministic(True) == prev
+        assert pa.decode_deterministic() is True
+        assert pa.set_decode_deterministic(False) is True
+        assert pa.decode_deterministic() is False
+    finally:
+        pa.set_decode_deterministic(prev)
+
+
 def test_version_and_status_strings(pa):
     from paged_kv_cache_257_gb300 import _native
     assert "sm_103a" in pa.version()

@@ -1,0 +1,147 @@
+"""Decode and append under CUDA graph capture.
+
+A serving loop launches the decode steps of a fixed batch shape from a
+captured graph, with each step's data copied into the captured buffers.
+These tests capture the library's calls (no allocation or synchronisation
+happens inside them when the output and workspace are given) and check
+the replays:
+- against the same calls run eagerly on the same inputs: bit for bit in
+  the deterministic schedule; in the default one, with 16-bit caches, an
+  item's last chunks go to whichever warp is free, so a warp's softmax
+  reference and sums can differ between runs at the level of bf16 rounding
+  of the probabilities (FP8 keeps a fixed schedule: bit for bit);
+- against the oracle, within the dtype's tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from harness import TOL, Case, assert_close, to_torch
+from oracle import attention as oatt
+from oracle import numerics
+from synth import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(case, q_store, tables, ctx):
+    kp, vp = case.oracle_pools()
+    return oatt.decode_attention_paged(q_store, kp, vp, tables, ctx, case.scale, case.kv_dtype, case.k_scale,
+                                       case.v_scale, q_dtype=case.q_dtype)
+
+
+@pytest.fixture(params=[False, True], ids=["balanced", "deterministic"])
+def schedule(pa, request):
+    prev = pa.set_decode_deterministic(request.param)
+    yield request.param
+    pa.set_decode_deterministic(prev)
+
+
+@pytest.mark.parametrize("kv,q,partition", [("bf16", "bf16", 256), ("fp8_e4m3", "bf16", 64), ("f16", "f16", -1)])
+def test_decode_replays_match_eager_and_oracle(pa, cuda, kv, q, partition, schedule):
+    # partition 256: the fused merge; 64: 47 partitions, the merge kernel; -1: unsplit
+    case = Case(batch=5, hq=16, hkv=4, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[3000, 17, 700, 1, 1234], seed=71)
+    desc = case.desc(pa)
+    kc, vc = case.gpu_pools(pa, cuda)
+    q_dev = to_torch(case.q_store, case.q_dtype, cuda)
+    bt = torch.from_numpy(case.tables).to(cuda)
+    cl = torch.from_numpy(case.ctx).to(cuda)
+    need = pa.decode_workspace_size(desc, case.batch, case.hq, case.max_blocks, partition)
+    ws = pa.new_workspace(need, cuda) if need else None
+    out = torch.empty((case.batch, case.hq, case.d), dtype=torch.float32, device=cuda)
+
+    def step():
+        pa.decode_attention(desc, q_dev, kc, vc, bt, cl, case.scale, partition=partition, workspace=ws, out=out)
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step()
+
+    # two rounds of new data through the captured buffers: queries and
+    # context lengths change (the tables stay valid for the shorter lengths)
+    for rnd in range(2):
+        q_new = workloads.cast(synth.normal_f32(72 + rnd, 1, case.batch * case.hq * case.d)
+                               .reshape(case.batch, case.hq, case.d), case.q_dtype)
+        ctx_new = np.maximum(case.ctx - np.array([rnd * 1000, 0, rnd * 300, 0, rnd * 7]), 0).astype(np.int32)
+        q_dev.copy_(to_torch(q_new, case.q_dtype, cuda))
+        cl.copy_(torch.from_numpy(ctx_new))
+        g.replay()
+        torch.cuda.synchronize()
+        got = out.clone()
+        step()                                       # the same calls, eagerly
+        torch.cuda.synchronize()
+        if schedule or kv == "fp8_e4m3":             # fixed chunk order: bit for bit
+            assert torch.equal(got, out), f"round {rnd}: graph replay differs from the eager call"
+        else:                                        # bf16 rounding of the probabilities
+            assert_close(got.cpu().numpy(), out.cpu().numpy().astype(np.float64), 2e-3, f"round {rnd} vs eager")
+        want = _oracle(case, q_new, case.tables, ctx_new)
+        assert_close(got.cpu().numpy(), want, TOL[kv], f"replay {rnd} {kv} P{partition}")
+
+
+def test_append_then_decode_replays(pa, cuda):
+    """One captured step appends a token to every sequence and decodes; each
+    replay writes the tokens and slots copied in before it."""
+    case = Case(batch=3, hq=8, hkv=2, d=128, bs=16, kv_dtype="bf16", q_dtype="bf16", ctx=[40, 16, 5], seed=73,
+                spare_blocks=6)
+    desc = case.desc(pa)
+    kc, vc = case.gpu_pools(pa, cuda)
+    # room for two more tokens per sequence: sequence 1 (16 tokens) needs a new block
+    tables = case.tables.copy()
+    used = {int(b) for s, c in enumerate(case.ctx) for b in tables[s, :-(-int(c) // case.bs)]}
+    free = [b for b in range(case.num_blocks) if b not in used]
+    for s, c in enumerate(case.ctx):
+        for j in range(-(-int(c) // case.bs), -(-(int(c) + 2) // case.bs)):
+            tables[s, j] = free.pop(0)
+    bt = torch.from_numpy(tables).to(cuda)
+    cl = torch.zeros(case.batch, dtype=torch.int32, device=cuda)
+    slots = torch.zeros(case.batch, dtype=torch.int64, device=cuda)
+    k_new = torch.zeros((case.batch, case.hkv, case.d), dtype=torch.bfloat16, device=cuda)
+    v_new = torch.zeros_like(k_new)
+    q_dev = to_torch(case.q_store, "bf16", cuda)
+    out = torch.empty((case.batch, case.hq, case.d), dtype=torch.float32, device=cuda)
+
+    def set_inputs(rnd):
+        """Round rnd appends position ctx + rnd of every sequence."""
+        pos = case.ctx + rnd
+        slot_np = np.array([tables[s, p // case.bs] * case.bs + p % case.bs for s, p in enumerate(pos)], np.int64)
+        kn = workloads.cast(synth.normal_f32(74, rnd, case.batch * case.hkv * case.d)
+                            .reshape(case.batch, case.hkv, case.d), "bf16")
+        vn = workloads.cast(synth.normal_f32(75, rnd, case.batch * case.hkv * case.d)
+                            .reshape(case.batch, case.hkv, case.d), "bf16")
+        slots.copy_(torch.from_numpy(slot_np))
+        k_new.copy_(to_torch(kn, "bf16", cuda))
+        v_new.copy_(to_torch(vn, "bf16", cuda))
+        cl.copy_(torch.from_numpy((pos + 1).astype(np.int32)))
+        return kn, vn
+
+    def step():
+        pa.kv_append(desc, k_new, v_new, slots, kc, vc)
+        pa.decode_attention(desc, q_dev, kc, vc, bt, cl, case.scale, partition=-1, out=out)
+
+    side = torch.cuda.Stream()
+    set_inputs(0)
+    with torch.cuda.stream(side):
+        step()                                       # warm-up (round 0's slots; the replay rewrites them)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step()
+
+    K = [numerics.to_f64(case.k_src[s], "bf16") for s in range(case.batch)]
+    V = [numerics.to_f64(case.v_src[s], "bf16") for s in range(case.batch)]
+    qf = numerics.to_f64(case.q_store, "bf16")
+    for rnd in range(2):
+        kn, vn = set_inputs(rnd)
+        g.replay()
+        torch.cuda.synchronize()
+        for s in range(case.batch):
+            K[s] = np.concatenate([K[s], numerics.to_f64(kn[s:s + 1], "bf16")])
+            V[s] = np.concatenate([V[s], numerics.to_f64(vn[s:s + 1], "bf16")])
+            want = oatt.decode_attention_contiguous(qf[s], K[s], V[s], case.scale)
+            assert_close(out[s].cpu().numpy(), want, TOL["bf16"], f"append+decode replay {rnd} seq {s}")
