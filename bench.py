@@ -292,8 +292,8 @@ class GpuWorkload:
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
-NCU_TRAFFIC = {"78c55ec0130ecd5a": {"gqa_bf16": 283_155_712 + 3_357_184,
-                                    "longctx_fp8": 1_074_031_104 + 7_497_472}}
+NCU_TRAFFIC = {"ad4488f2e69beece": {"gqa_bf16": 283_154_944 + 3_319_296,
+                                    "longctx_fp8": 1_074_071_296 + 7_793_152}}
 
 
 def captured_traffic(workload):
