@@ -286,24 +286,35 @@ class GpuWorkload:
 
 # DRAM bytes (read + write) of one decode_mma_kernel launch, from the ncu
 # captures summarised in profiles/decode_mma_<workload>.md.  They hold for the
-# kernel sources they were taken on (first 16 hex digits of the sha256 of the
-# files below, concatenated); after any change to them traffic is reported as
+# kernel code they were taken on (the fingerprint of the files below, see
+# _code_fingerprint); after any change to that code traffic is reported as
 # null until a new capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
-NCU_TRAFFIC = {"ad4488f2e69beece": {"gqa_bf16": 283_154_944 + 3_319_296,
+NCU_TRAFFIC = {"c95e6201be2f6e43": {"gqa_bf16": 283_154_944 + 3_319_296,
                                     "longctx_fp8": 1_074_071_296 + 7_793_152}}
 
 
-def captured_traffic(workload):
+def _code_fingerprint(paths):
+    """First 16 hex digits of the sha256 of the files' code with comments
+    and runs of white space removed, so that edits to comments alone keep
+    the recorded counters valid and any change to the code voids them."""
     import hashlib
+    import re
     root = os.path.dirname(os.path.abspath(__file__))
     h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
-        with open(os.path.join(root, f), "rb") as fh:
-            h.update(fh.read())
-    return NCU_TRAFFIC.get(h.hexdigest()[:16], {}).get(workload)
+    for f in paths:
+        with open(os.path.join(root, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(workload):
+    return NCU_TRAFFIC.get(_code_fingerprint(TRAFFIC_SOURCES), {}).get(workload)
 
 
 def copy_blocks_timing(pa, torch, w, device, pairs=4096):
