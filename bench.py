@@ -293,7 +293,9 @@ TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cach
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
 NCU_TRAFFIC = {"c95e6201be2f6e43": {"gqa_bf16": 283_154_944 + 3_319_296,
-                                    "longctx_fp8": 1_074_071_296 + 7_793_152}}
+                                    "longctx_fp8": 1_074_071_296 + 7_793_152,
+                                    "mha_f16": 671_302_912 + 3_274_752,
+                                    "prefix_bf16": 72_584_704 + 1_070_592}}
 
 
 def _code_fingerprint(paths):
