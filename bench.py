@@ -6,16 +6,19 @@ attention (decode kernel + split-context merge kernel).  Inputs are seeded
 and synthetic; the caches are built through the library before timing.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--partition P]
-                    [--window W] [--block-size 8|16|32] [--no-cpu-baseline]
+                    [--window W] [--block-size 8|16|32] [--no-cpu-baseline] [--no-workloads]
     python bench.py --impl reference ...     # the oracle on the host cores
 
-NAME is gqa_bf16 (the default), mha_f16, prefix_bf16 or longctx_fp8.
+NAME is longctx_fp8 (the default: the 70B-shaped 4 x 131072-token FP8
+cache, in 512-token partitions), gqa_bf16, mha_f16, prefix_bf16 or tiny.
 
 Prints one JSON line.  ``value`` is decode tokens/s (batch x steps / time)
 with every input resident in HBM; ``e2e`` is the same metric through the
 public API from pinned host buffers, copies included.  Between timed steps
 the caches rotate over replicas whose total size exceeds L2, so each step
-streams its KV from HBM.
+streams its KV from HBM.  Unless a partition, window or block size is
+forced, the line also carries ``workloads``: the device figures of every
+other workload, each on its own set-up and timed the same way.
 """
 
 import argparse
@@ -49,7 +52,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default="gqa_bf16")
+    p.add_argument("--workload", default="longctx_fp8")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--partition", type=int, default=None, help="tokens per partition (default: the workload's)")
     p.add_argument("--window", type=int, default=0,
@@ -57,7 +60,10 @@ def parse():
     p.add_argument("--block-size", type=int, default=None, choices=[8, 16, 32],
                    help="re-block gqa_bf16 / mha_f16 / longctx_fp8 (default: their 16-token blocks)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle baseline sample")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the device records of the other workloads (the line's \"workloads\" key)")
+    p.add_argument("--cpu-seconds", type=float, default=16.0,
+                   help="budget of the oracle baseline (half on one core, half on every core)")
     p.add_argument("--clock-probe-s", type=float, default=2.0,
                    help="seconds of untimed load before the timed steps, for the clock sampler")
     return p.parse_args()
@@ -591,89 +597,176 @@ def time_e2e_graph(wk, steps, warmup):
 
 
 # -------------------------------------------------------------- oracle arm
+#
+# The oracle timed on the host cores: bench's cpu_baseline leg and the
+# reference arm (--impl reference).  Workers are separate processes started
+# with `spawn` (never forked from a process that has touched the GPU), each
+# with one BLAS thread, each timing the oracle's paged decode over its own
+# share of the workload.  Long contexts are sampled: a worker attends the
+# first ORACLE_TOKEN_CAP tokens of its sequence and counts that call as the
+# matching fraction of a sequence-step.
 
-_ORACLE_SETUP = {}
+ORACLE_TOKEN_CAP = 8192
+_ONE_THREAD_ENV = {k: "1" for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
+                                     "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")}
 
 
-def oracle_setup(w_name):
-    """The oracle's own paged cache for a sample of the workload's sequences.
+def oracle_share(w_name, worker, n_workers, window=0):
+    """(sequence ids, token cap or None) of one worker's sample."""
+    from synth import workloads as wl
+    w = wl.make(w_name, BLOCK_SIZE)
+    cap = ORACLE_TOKEN_CAP if int(np.max(w.context_lens)) > 4 * ORACLE_TOKEN_CAP and window <= 0 else None
+    if cap is None and n_workers <= w.batch:
+        return list(range(worker, w.batch, n_workers)), None
+    return [worker % w.batch], cap
 
-    Small workloads keep every sequence; long ones keep sequence 0 (same
-    shapes, same block ids).  Built once per process, outside any timing."""
-    if w_name in _ORACLE_SETUP:
-        return _ORACLE_SETUP[w_name]
+
+def oracle_sample(w_name, seqs, cap, window=0):
+    """The oracle's own paged cache for sequences ``seqs`` of the workload (at
+    most their first ``cap`` tokens when ``cap`` is set).  The pool holds
+    only those sequences' blocks, in the workload's physical order and
+    sharing (ids renumbered), so the sample reads scattered blocks as the
+    full workload does.  Returns the inputs of decode_attention_paged and
+    the sequence-steps one call stands for."""
     from oracle import allocator as oalloc
     from oracle import cache as ocache
     from synth import workloads as wl
     w = wl.make(w_name, BLOCK_SIZE)
     if w.block_tables is None:
-        tables, ctx, new_slots = wl.build_prefix_tables(w, oalloc.BlockAllocator(w.num_blocks, w.alloc_seed))
+        tables, ctx, _ = wl.build_prefix_tables(w, oalloc.BlockAllocator(w.num_blocks, w.alloc_seed))
     else:
-        tables, ctx, new_slots = w.block_tables, w.context_lens.astype(np.int64), None
-    seqs = list(range(w.batch)) if int(np.sum(ctx)) <= 200_000 else [0]
-    kp = ocache.new_pool(w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim, w.kv_dtype)
-    vp = ocache.new_pool(w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim, w.kv_dtype)
+        tables, ctx = w.block_tables, w.context_lens.astype(np.int64)
+    bs = w.block_size
+    full = np.asarray([int(ctx[s]) for s in seqs], dtype=np.int64)
+    lens = np.minimum(full, cap) if cap else full
+    nblk = [-(-int(n) // bs) for n in lens]
+    used = sorted({int(tables[s, j]) for s, n in zip(seqs, nblk) for j in range(n)})
+    renum = {b: i for i, b in enumerate(used)}
+    t2 = np.zeros((len(seqs), max(1, max(nblk))), dtype=np.int32)
+    for i, (s, n) in enumerate(zip(seqs, nblk)):
+        t2[i, :n] = [renum[int(b)] for b in tables[s, :n]]
+    kp = ocache.new_pool(max(1, len(used)), w.n_kv_heads, bs, w.head_dim, w.kv_dtype)
+    vp = ocache.new_pool(max(1, len(used)), w.n_kv_heads, bs, w.head_dim, w.kv_dtype)
+    vals = [(wl.kv_tokens_f32(w, "k", s, 0, int(n)), wl.kv_tokens_f32(w, "v", s, 0, int(n)))
+            for s, n in zip(seqs, lens)]
     scales = (1.0, 1.0)
-    vals = {s: (wl.kv_tokens_f32(w, "k", s, 0, int(ctx[s])), wl.kv_tokens_f32(w, "v", s, 0, int(ctx[s])))
-            for s in seqs}
     if w.kv_dtype == "fp8_e4m3":
-        scales = (float(wl.fp8_scale_of(np.concatenate([vals[s][0].ravel() for s in seqs]))),
-                  float(wl.fp8_scale_of(np.concatenate([vals[s][1].ravel() for s in seqs]))))
-    for s in seqs:
-        n = int(ctx[s])
-        slots = ocache.slot_mapping(tables, [s] * n, range(n), w.block_size)
-        ocache.kv_append(kp, vp, wl.cast(vals[s][0], w.src_dtype), wl.cast(vals[s][1], w.src_dtype), slots,
-                         w.src_dtype, w.kv_dtype, *scales)
-    q = wl.cast(wl.queries_f32(w), w.q_dtype)[seqs]
-    _ORACLE_SETUP[w_name] = (w, seqs, q, kp, vp, tables[seqs], ctx[seqs], scales)
-    return _ORACLE_SETUP[w_name]
+        scales = (float(wl.fp8_scale_of(np.concatenate([k.ravel() for k, _ in vals]))),
+                  float(wl.fp8_scale_of(np.concatenate([v.ravel() for _, v in vals]))))
+    for i, ((k, v), n) in enumerate(zip(vals, lens)):
+        slots = ocache.slot_mapping(t2, [i] * int(n), range(int(n)), bs)
+        ocache.kv_append(kp, vp, wl.cast(k, w.src_dtype), wl.cast(v, w.src_dtype), slots, w.src_dtype,
+                         w.kv_dtype, *scales)
+    q = wl.cast(wl.queries_f32(w), w.q_dtype)[list(seqs)]
+    starts = np.maximum(lens - window, 0) if window > 0 else None
+    units = float(np.sum(lens / full))
+    return dict(w=w, q=q, kp=kp, vp=vp, tables=t2, ctx=lens, scales=scales, starts=starts, units=units)
 
 
-def oracle_step_sample(w_name, budget_s, window=0):
-    """Time the oracle's paged decode attention on the host for about ``budget_s``.
+def _oracle_call(s):
+    from oracle import attention as oatt  # test infrastructure: the oracle legs of this file only
+    w = s["w"]
+    oatt.decode_attention_paged(s["q"], s["kp"], s["vp"], s["tables"], s["ctx"], w.scale, w.kv_dtype,
+                                *s["scales"], q_dtype=w.q_dtype, context_starts=s["starts"])
 
-    Returns (decode tokens per second, sequence-steps run, seconds, sample text)."""
-    from oracle import attention as oatt  # test infrastructure: the CPU baseline leg only
-    w, seqs, q, kp, vp, tables, ctx, (ks, vs) = oracle_setup(w_name)
-    starts = np.maximum(ctx - window, 0) if window > 0 else None
-    t0 = time.perf_counter()
-    done = 0
-    while True:
-        oatt.decode_attention_paged(q, kp, vp, tables, ctx, w.scale, w.kv_dtype, ks, vs, q_dtype=w.q_dtype,
-                                    context_starts=starts)
-        done += len(seqs)
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = time.perf_counter() - t0
-    sample = (f"oracle decode_attention_paged (numpy, float64) over {len(seqs)} of {w.batch} sequences of "
-              f"{w_name} (their block tables and context lengths"
-              + (f", last {window} tokens" if window > 0 else "") + f"), {done} sequence-steps in {dt:.1f} s")
-    return done / dt, done, dt, sample
+
+def _oracle_worker(w_name, worker, n_workers, window, block_size, calls, warmup, budget_s, barrier_, queue):
+    """One spawned worker: set up its share, wait for the others, then time
+    ``calls`` oracle calls (or as many as fit in ``budget_s``)."""
+    global BLOCK_SIZE
+    BLOCK_SIZE = block_size
+    try:
+        seqs, cap = oracle_share(w_name, worker, n_workers, window)
+        s = oracle_sample(w_name, seqs, cap, window)
+        for _ in range(warmup):
+            _oracle_call(s)
+        barrier_.wait(timeout=900)
+        t0 = time.perf_counter()
+        done = 0
+        while (calls is not None and done < calls) or (calls is None and (done == 0 or
+                                                                            time.perf_counter() - t0 < budget_s)):
+            _oracle_call(s)
+            done += 1
+        queue.put((worker, done * s["units"], time.perf_counter() - t0, done, seqs, cap))
+    except BaseException as e:  # reported to the parent, which raises
+        queue.put((worker, None, repr(e), 0, [], None))
+
+
+def run_oracle(w_name, n_workers, calls=None, warmup=0, budget_s=None, window=0):
+    """The oracle's throughput on ``n_workers`` host cores: each worker a
+    spawned single-threaded process over its own share of the workload,
+    all timed together.  Returns (sequence-steps per second, seconds,
+    sequence-steps, sample text)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    saved = {k: os.environ.get(k) for k in _ONE_THREAD_ENV}
+    os.environ.update(_ONE_THREAD_ENV)              # children start with one BLAS thread
+    try:
+        queue, barrier_ = ctx.Queue(), ctx.Barrier(n_workers)
+        procs = [ctx.Process(target=_oracle_worker, args=(w_name, i, n_workers, window, BLOCK_SIZE, calls, warmup,
+                                                          budget_s, barrier_, queue)) for i in range(n_workers)]
+        for p in procs:
+            p.start()
+        res = [queue.get(timeout=1800) for _ in procs]
+        for p in procs:
+            p.join(timeout=60)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    bad = [r for r in res if r[1] is None]
+    if bad:
+        raise RuntimeError(f"oracle worker failed: {bad[0][2]}")
+    secs = max(r[2] for r in res)
+    units = sum(r[1] for r in res)
+    calls_done = sum(r[3] for r in res)
+    cap = res[0][5]
+    sample = (f"oracle decode_attention_paged (numpy, float64) in {n_workers} spawned single-threaded "
+              f"process(es), each over its share of {w_name}'s sequences (their block tables, context lengths"
+              + (f" capped at the first {cap} tokens, counted as {cap}/{int(max(wl_ctx(w_name)))} of a "
+                 f"sequence-step" if cap else "") + (f", last {window} tokens" if window > 0 else "")
+              + f"): {calls_done} calls, {units:.3f} sequence-steps in {secs:.1f} s")
+    return units / secs, secs, units, sample
+
+
+def wl_ctx(w_name):
+    from synth import workloads as wl
+    return wl.make(w_name, BLOCK_SIZE).context_lens
+
+
+def cpu_baseline(w_name, budget_s, window=0):
+    """The oracle on one core and on every core of the host, same sample."""
+    n = os.cpu_count() or 1
+    v1, s1, u1, sample1 = run_oracle(w_name, 1, budget_s=budget_s / 2, window=window)
+    vn, sn, un, samplen = run_oracle(w_name, n, budget_s=budget_s / 2, window=window)
+    return {"value": vn, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": samplen,
+            "value_all_cores": vn, "value_1thread": v1, "sample_1thread": sample1, **host_cpu()}
 
 
 def host_cpu():
     """The host's CPU model and logical core count."""
-    model = platform.processor() or platform.machine()
+    model = None
     try:
-        with open("/proc/cpuinfo") as f:
-            for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model"):
-                    model = line.split(":", 1)[1].strip()
-                    break
-    except OSError:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.split(":")[0].strip().lower() == "model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
         pass
-    return {"cpu_model": model, "nproc": os.cpu_count()}
-
-
-def oracle_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info()]
-        return max(n) if n else 1
-    except Exception:
-        return os.cpu_count() or 1
-
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    key = line.split(":")[0].strip().lower()
+                    if key in ("model name", "cpu model"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": f"{model or platform.machine()} ({platform.machine()})", "nproc": os.cpu_count()}
 
 # ----------------------------------------------------------- distributed
 
@@ -711,6 +804,45 @@ def job_rate(units_per_step, steps, world, local_ms):
     return units_per_step * steps * world / (t / 1e3), t
 
 
+def replicas_for(w):
+    """Cache replicas whose total exceeds L2 several times (one when a single
+    copy already does), so that every step streams its KV from HBM."""
+    per = w.num_blocks * w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes * 2
+    return max(1, min(4, math.ceil(3 * L2_BYTES / per))), per
+
+
+OTHER_WORKLOADS = ("gqa_bf16", "mha_f16", "prefix_bf16", "tiny", "longctx_fp8")
+
+
+def workload_record(name, device, steps, warmup):
+    """Device-side figures of one more workload (its own set-up, the same
+    timing as the headline's, no end-to-end loop and no clock probe)."""
+    import torch
+    from synth import workloads as wl
+    w = wl.make(name, BLOCK_SIZE)
+    replicas, per = replicas_for(w)
+    wk = GpuWorkload(name, device, replicas)
+    total_ms, dec_ms, app_ms, launches = time_device(wk, steps, warmup)
+    peak = measured_peak()[0]
+    step_s = total_ms / 1e3 / steps
+    dec_s = statistics.mean(dec_ms) / 1e3
+    rec = {"batch": w.batch, "kv_dtype": w.kv_dtype, "kv_tokens": wk.kv_tokens, "kv_bytes": wk.kv_bytes,
+           "partition_size": wk.resolved_partition, "tokens_per_s": w.batch / step_s, "ms_per_step": step_s * 1e3,
+           "decode_us": _stats_us(dec_ms), "kv_gbs": wk.kv_bytes / dec_s / 1e9,
+           "frac": wk.kv_bytes / dec_s / 1e9 / peak, "traffic": captured_traffic(name),
+           "kv_gbs_step": wk.kv_bytes / step_s / 1e9, "gpu_launches": launches,
+           "l2": (f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)"
+                  if replicas * per > L2_BYTES else f"KV ({per / 2**10:.0f} KiB) fits in L2: launch-bound")}
+    if wk.unique_kv_bytes != wk.kv_bytes:
+        rec["unique_kv_gbs"] = wk.unique_kv_bytes / dec_s / 1e9
+        rec["unique_frac"] = rec["unique_kv_gbs"] / peak
+    if app_ms:
+        rec["append_us"] = dict(_stats_us(app_ms), tokens=w.append_tokens)
+    del wk
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     global BLOCK_SIZE
     args = parse()
@@ -730,9 +862,7 @@ def main():
     torch.cuda.set_device(device)
     from synth import workloads as wl
     w = wl.make(args.workload, BLOCK_SIZE)
-    # enough replicas of the caches that their total exceeds L2 several times
-    per = w.num_blocks * w.n_kv_heads * w.block_size * w.head_dim * w.kv_elem_bytes * 2
-    replicas = max(1, min(4, math.ceil(3 * L2_BYTES / per)))
+    replicas, per = replicas_for(w)
     wk = GpuWorkload(args.workload, device, replicas, args.partition, args.window)
     with ClockSampler(local) as clk:
         total_ms, dec_ms, app_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
@@ -786,10 +916,18 @@ def main():
     if w.prefix_len and rank == 0:
         line["prefix_cache"] = prefix_cache_host_timing(wk.pa, w)
     line["copy_blocks"] = copy_blocks_timing(wk.pa, torch, w, device)
+    del wk
+    torch.cuda.empty_cache()
+    # the other workloads, each measured the same way on its own set-up
+    plain = args.partition is None and args.window <= 0 and args.block_size is None
+    if plain and not args.no_workloads:
+        recs = {}
+        for name in OTHER_WORKLOADS:
+            if name != args.workload:
+                recs[name] = workload_record(name, device, args.steps, args.warmup)
+        line["workloads"] = recs
     if rank == 0 and not args.no_cpu_baseline:
-        v, done, dt, sample = oracle_step_sample(args.workload, args.cpu_seconds, args.window)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
-                                "sample": sample, **host_cpu()}
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds, args.window)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if _dist is not None:
@@ -798,28 +936,23 @@ def main():
 
 
 def run_reference(args):
-    """The oracle as the reference arm: K timed steps, each a bounded sample of the workload."""
+    """The oracle as the reference arm on every host core: W untimed calls,
+    then K timed calls per worker, each call a bounded sample of the
+    workload (the worker's share of the sequences)."""
     from synth import workloads as wl
     w = wl.make(args.workload, BLOCK_SIZE)
-    per_step = max(1.0, min(10.0, 60.0 / max(1, args.steps)))
-    for _ in range(args.warmup):
-        oracle_step_sample(args.workload, 0.0, args.window)
-    t0 = time.perf_counter()
-    total = 0
-    sample = ""
-    for _ in range(args.steps):
-        _, done, _, sample = oracle_step_sample(args.workload, per_step, args.window)
-        total += done
-    dt = time.perf_counter() - t0
-    value = total / dt
+    n = os.cpu_count() or 1
+    value, secs, units, sample = run_oracle(args.workload, n, calls=args.steps, warmup=args.warmup,
+                                            window=args.window)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": secs * 1e3 / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, "batch": w.batch, "n_q_heads": w.n_q_heads,
                        "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                       "kv_dtype": w.kv_dtype, "parallelism": "host cores",
+                       "kv_dtype": w.kv_dtype, "q_dtype": w.q_dtype, "partition_size": w.partition_size or None,
+                       "parallelism": f"{n} host processes",
                        **({"window": args.window} if args.window > 0 else {})},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle",
                              "sample": sample, **host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

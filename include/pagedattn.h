@@ -32,6 +32,9 @@
  *     unspecified.  pa_read_device_status() reads the word back.
  *   - Device kernels never trap and never wait without a time limit; a
  *     wait that runs out sets PA_DEVFLAG_TIMEOUT and the kernel returns.
+ *     When PA_DEVFLAG_TIMEOUT is set, the whole output of that call is
+ *     undefined (not only the rows whose wait ran out: a CTA that gave up
+ *     may reuse on-chip buffers that late copies still land in).
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
@@ -268,7 +271,11 @@ pa_status pa_decode_attention_window(const pa_cache_desc* cache, const void* q, 
  *     batch, or pa_decode_attention with a caller-owned workspace).
  *   - The first call on a device looks up the array's device address with
  *     that device current and zero-fills it, synchronising the device; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The same set-up runs
+ *     again on the first call after the device's context was destroyed
+ *     (cudaDeviceReset), since the new context holds the array elsewhere.
+ *   - PA_ERR_INVALID for a null input or output pointer when the call needs
+ *     the array (every other check is pa_decode_attention's).
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents; each call clears the merge counters it needs on its
  *     stream before the kernels.  Calls whose kernels overlap on the GPU

@@ -204,20 +204,22 @@ def decode_attention(desc, q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
-def decode_attention_noalloc(desc, q, k_cache, v_cache, block_tables, context_lens, scale, partition=0, out=None,
-                             out_dtype=None, status=None, stream=None):
+def decode_attention_noalloc(desc, q, k_cache, v_cache, block_tables, context_lens, scale, out, partition=0,
+                             status=None, stream=None):
     """``pa_decode_attention_noalloc``: decode attention with the library's static workspace.
 
-    For callers that must not allocate device memory (the library's own array
-    of 8 MiB per GPU replaces the workspace); ``out`` must then be passed in.
-    Raises NativeError("PA_ERR_RANGE") when the problem's workspace does not fit.
+    For callers that must not allocate device memory: the library's own array
+    of 8 MiB per GPU replaces the workspace, and this wrapper allocates
+    nothing either, so ``out`` ([batch, num_q_heads, head_dim], f32 / f16 /
+    bf16) is required.  Raises NativeError("PA_ERR_RANGE") when the
+    problem's workspace does not fit the array.
     """
     _need(q, "q")
     _need(block_tables, "block_tables", torch.int32)
     _need(context_lens, "context_lens", torch.int32)
-    batch, hq, d = q.shape
     if out is None:
-        out = torch.empty((batch, hq, d), dtype=TORCH_STORAGE[out_dtype or "f32"], device=q.device)
+        raise ValueError("decode_attention_noalloc allocates nothing: pass the output tensor as out")
+    batch, hq, d = q.shape
     _need(out, "out")
     c = desc.c()
     st = lib().pa_decode_attention_noalloc(ctypes.byref(c), _ptr(q), DTYPE[_dtype_of(q, "q")], hq, _ptr(k_cache),

@@ -9,6 +9,7 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "decode.h"
@@ -21,26 +22,70 @@ namespace {
 static_assert(PA_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte alignment");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
+// The array's device address belongs to one CUDA context: after a
+// cudaDeviceReset the device's next context holds the array elsewhere.
+// Each device's entry records the context it was looked up in (its driver
+// id), so a new context is noticed and the address asked for again.
+struct ScratchEntry {
+    unsigned long long ctx_id = 0;
+    void* ptr = nullptr;
+};
+
 std::mutex g_mutex;
-std::vector<void*> g_scratch_ptr;   // device address of the array, per device (null: not set up)
+std::vector<ScratchEntry> g_scratch;   // per device
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver id of the calling thread's current context (0 if none answers).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Device address of the array on the current device.  In host code the
 // array's name stands for a host-side shadow, never the device memory, so
-// the address is asked of the runtime once per device (with that device
-// current) and cached; the array is also zero-filled then.
+// the address is asked of the runtime with the device current, once per
+// device and context, and cached; the array is zero-filled then.
 pa_status scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    unsigned long long ctx = current_context_id();
+    if (ctx == 0) {   // no context current in this thread yet: the runtime makes the device's current
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return PA_ERR_CUDA;
+        ctx = current_context_id();
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (dev >= static_cast<int>(g_scratch_ptr.size())) g_scratch_ptr.resize(dev + 1, nullptr);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (dev >= static_cast<int>(g_scratch.size())) g_scratch.resize(dev + 1);
+    ScratchEntry& e = g_scratch[dev];
+    if (e.ptr == nullptr || e.ctx_id != ctx) {
+        e.ptr = nullptr;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
         if (cudaMemset(p, 0, PA_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return PA_ERR_CUDA;
         if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        e.ptr = p;
+        e.ctx_id = ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = e.ptr;
     return PA_OK;
 }
 
@@ -55,7 +100,8 @@ extern "C" pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, con
     const size_t need = pa_decode_workspace_size(cache, batch, num_q_heads, max_blocks_per_seq, partition_size);
     if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_RANGE;
     void* ws = nullptr;
-    if (need > 0 && q && k_cache && v_cache && block_tables && context_lens && out) {
+    if (need > 0) {
+        if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
         pa_status st = scratch_address(&ws);
         if (st != PA_OK) return st;
         // The array keeps the previous call's contents.  Its front holds the

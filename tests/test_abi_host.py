@@ -201,6 +201,29 @@ def test_decode_rejects_bad_arguments_before_any_launch(pa):
     assert _call_decode(pa, pa.CacheDesc(1024, 16, 8, 128, "fp8_e4m3", 0.0, 1.0)) == 1
 
 
+def test_noalloc_rejects_null_pointers_and_oversized_problems_on_the_host(pa):
+    """The allocation-free entry point answers before any CUDA call: a null
+    input or output of a split call is PA_ERR_INVALID, a workspace beyond
+    its array PA_ERR_RANGE."""
+    from paged_kv_cache_257_gb300 import _native
+    lib = _native.lib()
+    c = pa.CacheDesc(1024, 16, 8, 128, "bf16").c()
+    assert pa.decode_workspace_size(pa.CacheDesc(1024, 16, 8, 128, "bf16"), 2, 32, 64, 256) > 0
+
+    def call(**o):
+        a = dict(q=4096, kc=4096, vc=4096, bt=4096, cl=4096, out=4096, part=256, batch=2, mb=64)
+        a.update(o)
+        return lib.pa_decode_attention_noalloc(ctypes.byref(c), a["q"], 2, 32, a["kc"], a["vc"], a["bt"], a["mb"],
+                                               a["cl"], a["batch"], 0.088, a["part"], a["out"], 0, None, None)
+    for name in ("q", "kc", "vc", "bt", "cl", "out"):
+        assert call(**{name: None}) == 1, name
+    big = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
+    assert pa.decode_workspace_size(big, 4, 64, 8192, 512) > _native.NOALLOC_SCRATCH_BYTES
+    cb = big.c()
+    assert lib.pa_decode_attention_noalloc(ctypes.byref(cb), 4096, 2, 64, 4096, 4096, 4096, 8192, 4096, 4, 0.088,
+                                           512, 4096, 0, None, None) == 3
+
+
 def test_append_rejects_bad_arguments(pa):
     from paged_kv_cache_257_gb300 import _native
     lib = _native.lib()
