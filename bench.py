@@ -267,13 +267,14 @@ class GpuWorkload:
             return None, None, None
         return dev(k), dev(v), torch.from_numpy(np.asarray(slots, dtype=np.int64)).to(self.device)
 
-    def step(self, r, ev=None):
+    def step(self, r, ev=None, decode_only=False):
         """One step on cache replica r; ``ev``: None or four events (append
-        start, end, decode start, end).  Returns the kernels it launched."""
+        start, end, decode start, end); ``decode_only`` leaves the append
+        out.  Returns the kernels it launched."""
         pa = self.pa
         kc, vc = self.pools[r % len(self.pools)]
         n = 0
-        if self.new_k is not None:
+        if self.new_k is not None and not decode_only:
             if ev is not None:
                 ev[0].record()
             pa.kv_append(self.desc, self.new_k, self.new_v, self.new_slots, kc, vc)
@@ -295,7 +296,8 @@ class GpuWorkload:
 # kernel code they were taken on (the fingerprint of the files below, see
 # _code_fingerprint); after any change to that code traffic is reported as
 # null until a new capture is recorded here.
-TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/common.cuh",
+TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/decode_warp.cu",
+                   "paged_kv_cache_257_gb300/csrc/mma_chunk.cuh", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
 NCU_TRAFFIC = {"c95e6201be2f6e43": {"gqa_bf16": 283_154_944 + 3_319_296,
@@ -389,56 +391,87 @@ def prefix_cache_host_timing(pa, w):
     return out
 
 
-def time_device(wk, steps, warmup, probe_s=0.0):
-    """Timed region: barrier + synchronize, K steps, synchronize.  Then K
-    more steps with events around the append and the decode.  Returns (total
-    ms of the timed region, decode ms per step, append ms per step or [],
-    launches in the timed region).
+def capture(wk, fn):
+    """A CUDA graph of the library calls ``fn`` makes (captured on a side
+    stream; replayed on the current one).  Returns (graph, fn's result)."""
+    torch = wk.torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        res = fn()
+    torch.cuda.current_stream().wait_stream(side)
+    return g, res
 
-    ``probe_s`` seconds of extra untimed steps run first so that the clock
+
+def replay_ms(wk, g):
+    """Device time of one replay of ``g`` (CUDA events on the current stream,
+    synchronised on both sides)."""
+    torch = wk.torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def time_device(wk, steps, warmup, probe_s=0.0):
+    """The device-side timings of a workload.
+
+    W eager warm-up steps, then the K timed steps launched as one CUDA graph
+    (so that the host's launch rate never paces the GPU), bracketed by a
+    barrier and synchronisation; then a graph of K decode launches alone,
+    whose replay time / K is the decode's average launch duration; then the
+    same K steps again, launched eagerly with events around each append and
+    decode (per-launch spread; the events and the host's launches add gaps).
+
+    Returns (total ms of the timed steps, decode ms per launch in the
+    decode-only region, evented decode ms per step, evented append ms per
+    step or [], kernels launched in the timed region).
+
+    ``probe_s`` seconds of extra untimed replays run first so that the clock
     sampler (nvidia-smi, 200 ms period) sees the GPU under this load."""
     torch = wk.torch
     for i in range(warmup):
         wk.step(i)
     torch.cuda.synchronize()
-    t0, i = time.perf_counter(), warmup
+    g_steps, launches = capture(wk, lambda: sum(wk.step(warmup + i) for i in range(steps)))
+    g_dec, _ = capture(wk, lambda: [wk.step(warmup + i, decode_only=True) for i in range(steps)])
+    g_steps.replay()
+    g_dec.replay()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     while time.perf_counter() - t0 < probe_s:
-        wk.step(i)
-        i += 1
-        if i % 256 == 0:
-            torch.cuda.synchronize()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    launches = 0
-    start.record()
-    for i in range(steps):
-        launches += wk.step(warmup + i)
-    end.record()
-    torch.cuda.synchronize()
-    total_ms = start.elapsed_time(end)
-    # the same steps again with events around each kernel, for per-kernel
-    # durations (the events add time between kernels, so not in the total)
+        g_steps.replay()
+        torch.cuda.synchronize()
+    total_ms = replay_ms(wk, g_steps)
+    dec_launch_ms = replay_ms(wk, g_dec) / steps
+    del g_steps, g_dec
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for i in range(steps):
         wk.step(warmup + i, ev[i])
     torch.cuda.synchronize()
     dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
     app_ms = [e[0].elapsed_time(e[1]) for e in ev] if wk.new_k is not None else []
-    return total_ms, dec_ms, app_ms, launches
+    return total_ms, dec_launch_ms, dec_ms, app_ms, launches
 
 
 def time_decode_no_flush(wk, steps):
-    """Decode durations with one cache replica reused step after step (its
-    KV stays in L2 as far as it fits), after a warm-up step."""
-    torch = wk.torch
-    wk.step(0)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    for i in range(steps):
-        wk.step(0, ev[i])
-    torch.cuda.synchronize()
-    return [e[2].elapsed_time(e[3]) for e in ev]
+    """Decode average launch duration with one cache replica reused launch
+    after launch (its KV stays in L2 as far as it fits): a graph of K decode
+    launches on replica 0, after a warm-up replay."""
+    g, _ = capture(wk, lambda: [wk.step(0, decode_only=True) for _ in range(steps)])
+    g.replay()
+    wk.torch.cuda.synchronize()
+    return replay_ms(wk, g) / steps
+
+
+DECODE_US_NOTE = ("launch_avg: K decode launches replayed from one CUDA graph, region time / K (the roofline's "
+                  "duration); mean/median/min: the same launches made eagerly with CUDA events around each "
+                  "(they include the events' and the host's launch gaps)")
 
 
 def _stats_us(ms):
@@ -822,13 +855,14 @@ def workload_record(name, device, steps, warmup):
     w = wl.make(name, BLOCK_SIZE)
     replicas, per = replicas_for(w)
     wk = GpuWorkload(name, device, replicas)
-    total_ms, dec_ms, app_ms, launches = time_device(wk, steps, warmup)
+    total_ms, dec_launch_ms, dec_ms, app_ms, launches = time_device(wk, steps, warmup)
     peak = measured_peak()[0]
     step_s = total_ms / 1e3 / steps
-    dec_s = statistics.mean(dec_ms) / 1e3
+    dec_s = dec_launch_ms / 1e3
     rec = {"batch": w.batch, "kv_dtype": w.kv_dtype, "kv_tokens": wk.kv_tokens, "kv_bytes": wk.kv_bytes,
            "partition_size": wk.resolved_partition, "tokens_per_s": w.batch / step_s, "ms_per_step": step_s * 1e3,
-           "decode_us": _stats_us(dec_ms), "kv_gbs": wk.kv_bytes / dec_s / 1e9,
+           "decode_us": dict(_stats_us(dec_ms), launch_avg=dec_launch_ms * 1e3, note=DECODE_US_NOTE),
+           "kv_gbs": wk.kv_bytes / dec_s / 1e9,
            "frac": wk.kv_bytes / dec_s / 1e9 / peak, "traffic": captured_traffic(name),
            "kv_gbs_step": wk.kv_bytes / step_s / 1e9, "gpu_launches": launches,
            "l2": (f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)"
@@ -865,7 +899,8 @@ def main():
     replicas, per = replicas_for(w)
     wk = GpuWorkload(args.workload, device, replicas, args.partition, args.window)
     with ClockSampler(local) as clk:
-        total_ms, dec_ms, app_ms, launches = time_device(wk, args.steps, args.warmup, args.clock_probe_s)
+        total_ms, dec_launch_ms, dec_ms, app_ms, launches = time_device(wk, args.steps, args.warmup,
+                                                                       args.clock_probe_s)
     no_flush_ms = time_decode_no_flush(wk, args.steps)
     eager_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup)
     try:
@@ -876,7 +911,7 @@ def main():
     value, total_ms = job_rate(w.batch, args.steps, world, total_ms)
     e2e_value, e2e_ms = job_rate(w.batch, args.steps, world, e2e_ms)
     eager_value, eager_ms = job_rate(w.batch, args.steps, world, eager_ms)
-    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    dec_avg_s = dec_launch_ms / 1e3
     peak, peak_src = measured_peak()
     achieved = wk.kv_bytes / dec_avg_s / 1e9
     step_s = total_ms / 1e3 / args.steps
@@ -896,9 +931,11 @@ def main():
         "kv_tokens_per_s": wk.kv_tokens * world / step_s,
         "kv_gbs": wk.kv_bytes * world / step_s / 1e9,
         "decode_kernel_us": dec_avg_s * 1e6,
-        "decode_us": dict(_stats_us(dec_ms), no_flush_median=statistics.median(no_flush_ms) * 1e3,
+        "decode_us": dict(_stats_us(dec_ms), launch_avg=dec_launch_ms * 1e3, note=DECODE_US_NOTE,
+                          no_flush_launch_avg=no_flush_ms * 1e3,
                           no_flush_note="one replica reused: its KV stays in L2 as far as it fits"),
         "roofline": {"bound": "hbm", "kernel": "paged decode (decode + split merge)", "achieved": achieved,
+                     "duration": "decode_us.launch_avg: a CUDA-graph region of K decode launches / K",
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": captured_traffic(args.workload), "traffic_of": "one decode_mma_kernel launch (ncu)",
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes,

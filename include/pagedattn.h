@@ -304,6 +304,26 @@ pa_status pa_decode_attention_noalloc(const pa_cache_desc* cache, const void* q,
 void pa_set_decode_deterministic(int32_t on);
 int32_t pa_get_decode_deterministic(void);
 
+/* Which tensor-core decode kernel serves every later decode call of the
+ * process.  The pages have no counterpart: both compute the same attention
+ * (within the tolerances above) and differ only in how work items map to
+ * warps.
+ *   PA_DECODE_KERNEL_AUTO (default): the library picks per call: one warp
+ *     per work item when partitions are at least 512 tokens and the grid
+ *     holds at least two work items per warp slot of the GPU (20 per SM),
+ *     else one CTA of four warps per work item.
+ *   PA_DECODE_KERNEL_CTA: always a CTA of four warps per work item (an
+ *     item's chunks split among the warps, whose states are merged).
+ *   PA_DECODE_KERNEL_WARP: always one warp per work item.
+ * Calls on the CUDA-core kernel are unaffected.  Process-wide, like
+ * pa_set_decode_deterministic; PA_ERR_INVALID for another value.
+ * pa_get_decode_kernel returns the current setting. */
+#define PA_DECODE_KERNEL_AUTO 0
+#define PA_DECODE_KERNEL_CTA 1
+#define PA_DECODE_KERNEL_WARP 2
+pa_status pa_set_decode_kernel(int32_t kernel);
+int32_t pa_get_decode_kernel(void);
+
 /* Wait for `stream`, copy the device status word to *flags_out (may be
  * NULL) and, if `reset` is non-zero, zero it.  Returns PA_ERR_DEVICE_FLAG
  * if any flag was set, PA_OK otherwise. */

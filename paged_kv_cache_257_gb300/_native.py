@@ -24,6 +24,7 @@ DEVFLAG_BLOCK_RANGE = 2
 DEVFLAG_CONTEXT_RANGE = 4
 DEVFLAG_TIMEOUT = 8
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024   # PA_NOALLOC_SCRATCH_BYTES
+DECODE_KERNEL = {"auto": 0, "cta": 1, "warp": 2}   # PA_DECODE_KERNEL_*
 
 
 class CacheDescC(ctypes.Structure):
@@ -60,6 +61,8 @@ SIGNATURES = {
     "pa_read_device_status": (ctypes.c_int, [c_void_p, P_int32, c_int32, c_void_p]),
     "pa_set_decode_deterministic": (None, [c_int32]),
     "pa_get_decode_deterministic": (c_int32, []),
+    "pa_set_decode_kernel": (ctypes.c_int, [c_int32]),
+    "pa_get_decode_kernel": (c_int32, []),
     "pa_alloc_create": (ctypes.c_int, [c_int32, c_uint64, ctypes.POINTER(c_void_p)]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_alloc_num_blocks": (c_int32, [c_void_p]),

@@ -246,6 +246,24 @@ def decode_deterministic():
     return bool(lib().pa_get_decode_deterministic())
 
 
+def set_decode_kernel(kernel):
+    """``pa_set_decode_kernel``: "auto" (the library picks per call), "cta"
+    (a CTA of four warps per work item) or "warp" (one warp per work item)
+    for every later tensor-core decode call of the process.  Returns the
+    previous setting."""
+    from ._native import DECODE_KERNEL
+    names = {v: k for k, v in DECODE_KERNEL.items()}
+    prev = names[int(lib().pa_get_decode_kernel())]
+    check("pa_set_decode_kernel", lib().pa_set_decode_kernel(DECODE_KERNEL[kernel]))
+    return prev
+
+
+def decode_kernel():
+    """The current ``pa_set_decode_kernel`` setting."""
+    from ._native import DECODE_KERNEL
+    return {v: k for k, v in DECODE_KERNEL.items()}[int(lib().pa_get_decode_kernel())]
+
+
 def new_workspace(nbytes, device="cuda"):
     """A zero-filled decode workspace (the library keeps its counters zero between calls)."""
     return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
@@ -372,7 +390,7 @@ class BlockAllocator:
 __all__ = ["CacheDesc", "BlockAllocator", "AllocError", "NativeError", "version", "dtype_size",
            "kv_bytes_per_token", "compute_slot_mapping", "kv_append", "copy_blocks", "partition_size", "plan_partition",
            "PrefixCache",
-           "decode_workspace_size", "decode_attention", "decode_attention_noalloc", "new_status", "new_workspace", "read_device_status"]
+           "decode_workspace_size", "decode_attention", "decode_attention_noalloc", "set_decode_kernel", "decode_kernel", "new_status", "new_workspace", "read_device_status"]
 
 
 class PrefixCache:

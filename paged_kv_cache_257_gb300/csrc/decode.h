@@ -42,6 +42,12 @@ constexpr int kHeadsPerCta = 8;
 #define PA_DECODE_MIN_CTAS 5
 #endif
 
+// CTAs (one warp each) of the warp-per-item decode kernel resident per SM
+// (its register budget is sized for this many).
+#ifndef PA_DECODE_WARP_MIN_CTAS
+#define PA_DECODE_WARP_MIN_CTAS 20
+#endif
+
 // Up to this many partitions per sequence the decode kernel merges them itself.
 constexpr int kFusedMergeMaxParts = 16;
 
@@ -59,6 +65,11 @@ pa_status check_cache_desc(const pa_cache_desc* c);
 // Tensor-core kernel: 16-bit or FP8 cache, head_dim 128, 16-bit queries.
 bool mma_path_supported(const DecodeArgs& a);
 pa_status launch_decode_mma(const DecodeArgs& a, cudaStream_t stream);
+
+// Warp-per-item tensor-core kernel: the same cases as the CTA-per-item
+// kernel; chosen when work items are many and long (warp_path_preferred).
+pa_status launch_decode_warp(const DecodeArgs& a, cudaStream_t stream);
+bool warp_path_preferred(const DecodeArgs& a);
 
 // CUDA-core kernel: every supported combination.
 pa_status launch_decode_simt(const DecodeArgs& a, cudaStream_t stream);

@@ -14,6 +14,7 @@ namespace {
 constexpr int kMaxParts = 32768;
 
 std::atomic<int32_t> g_deterministic{0};   // pa_set_decode_deterministic
+std::atomic<int32_t> g_kernel{PA_DECODE_KERNEL_AUTO};   // pa_set_decode_kernel
 
 // Workspace layout of a split call: merge tickets, partial outputs and
 // partial (max, sum) pairs.  An unsplit call needs none.
@@ -138,6 +139,20 @@ size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q
     return w.tickets_bytes;
 }
 
+// Kernel choice for the tensor-core path.  One warp streams an item about
+// four times slower than a CTA of four warps, but it pays no pipeline fill
+// of its own while other warps stream and no cross-warp merge; that wins
+// when the items are long (partitions of 512 tokens or more) and at least
+// two waves of them cover every warp slot of the GPU.  The item count here
+// is the grid's upper bound (every sequence at the table's capacity).
+bool warp_path_preferred(const DecodeArgs& a) {
+    if (a.partition_size < 512) return false;
+    const int64_t n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
+    const int64_t items = static_cast<int64_t>(a.max_parts) * a.num_kv_heads * n_hg * a.batch;
+    const int64_t slots = static_cast<int64_t>(PA_DECODE_WARP_MIN_CTAS) * std::max(sm_count(), 1);
+    return items >= 2 * slots;
+}
+
 }  // namespace pa
 
 extern "C" size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
@@ -216,7 +231,13 @@ extern "C" pa_status pa_decode_attention_window(const pa_cache_desc* cache, cons
     a.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream_);
-    st = mma_path_supported(a) ? launch_decode_mma(a, s) : launch_decode_simt(a, s);
+    if (!mma_path_supported(a))
+        st = launch_decode_simt(a, s);
+    else {
+        const int32_t k = g_kernel.load(std::memory_order_relaxed);
+        const bool warp = k == PA_DECODE_KERNEL_WARP || (k == PA_DECODE_KERNEL_AUTO && warp_path_preferred(a));
+        st = warp ? launch_decode_warp(a, s) : launch_decode_mma(a, s);
+    }
     if (st == PA_OK && parts > 1 && !a.fused_merge) st = launch_decode_reduce(a, s);
     return st;
 }
@@ -235,3 +256,12 @@ extern "C" pa_status pa_decode_attention(const pa_cache_desc* cache, const void*
 extern "C" void pa_set_decode_deterministic(int32_t on) { g_deterministic.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 extern "C" int32_t pa_get_decode_deterministic(void) { return g_deterministic.load(std::memory_order_relaxed); }
+
+extern "C" pa_status pa_set_decode_kernel(int32_t kernel) {
+    if (kernel != PA_DECODE_KERNEL_AUTO && kernel != PA_DECODE_KERNEL_CTA && kernel != PA_DECODE_KERNEL_WARP)
+        return PA_ERR_INVALID;
+    g_kernel.store(kernel, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+extern "C" int32_t pa_get_decode_kernel(void) { return g_kernel.load(std::memory_order_relaxed); }

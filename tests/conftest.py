@@ -33,3 +33,12 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     return torch.device("cuda:0")
+
+
+@pytest.fixture
+def kernel(request, pa):
+    """Pin the tensor-core decode kernel ("cta" or "warp", from the test's
+    parameter) for one test, then restore the process setting."""
+    prev = pa.set_decode_kernel(request.param)
+    yield request.param
+    pa.set_decode_kernel(prev)

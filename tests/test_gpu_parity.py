@@ -39,26 +39,29 @@ def test_tiny_workload(pa, cuda):
 
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("f16", "f16"), ("fp8_e4m3", "bf16"), ("fp8_e4m3", "f16")])
 @pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8), (16, 2), (4, 2), (32, 2)])
-def test_tensor_core_path_ragged(pa, cuda, kv, q, hq, hkv):
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_tensor_core_path_ragged(pa, cuda, kernel, kv, q, hq, hkv):
     case = Case(batch=len(RAGGED), hq=hq, hkv=hkv, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=RAGGED, seed=hq + hkv)
     got, expect = _run(pa, cuda, case)
-    assert_close(got, expect, TOL[kv], f"{kv} G={hq // hkv}")
+    assert_close(got, expect, TOL[kv], f"{kv} G={hq // hkv} {kernel}")
 
 
 @pytest.mark.parametrize("partition", [-1, 16, 64, 256, 512, 0])
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp8_e4m3", "bf16"), ("f32", "f32")])
-def test_partition_invariance(pa, cuda, partition, kv, q):
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_partition_invariance(pa, cuda, kernel, partition, kv, q):
     case = Case(batch=5, hq=8, hkv=2, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[3000, 1, 511, 512, 513], seed=7)
     got, expect = _run(pa, cuda, case, partition=partition)
-    assert_close(got, expect, TOL[kv], f"P={partition}")
+    assert_close(got, expect, TOL[kv], f"P={partition} {kernel}")
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp8_e4m3", "bf16"), ("f16", "f32"), ("f32", "f32")])
-def test_block_sizes(pa, cuda, bs, kv, q):
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_block_sizes(pa, cuda, kernel, bs, kv, q):
     case = Case(batch=6, hq=8, hkv=4, d=128, bs=bs, kv_dtype=kv, q_dtype=q, ctx=[1, 7, 8, 9, 31, 700], seed=bs)
     got, expect = _run(pa, cuda, case, partition=64)
-    assert_close(got, expect, TOL[kv], f"bs={bs}")
+    assert_close(got, expect, TOL[kv], f"bs={bs} {kernel}")
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])

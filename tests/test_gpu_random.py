@@ -37,8 +37,9 @@ def _config(seed):
                 starts=starts)
 
 
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
 @pytest.mark.parametrize("seed", range(100))
-def test_random_configuration(pa, cuda, seed):
+def test_random_configuration(pa, cuda, kernel, seed):
     c = _config(seed)
     case = Case(batch=c["batch"], hq=c["hq"], hkv=c["hkv"], d=c["d"], bs=c["bs"], kv_dtype=c["kv"], q_dtype=c["q"],
                 ctx=c["ctx"], seed=2000 + seed)
@@ -53,4 +54,4 @@ def test_random_configuration(pa, cuda, seed):
     kp, vp = case.oracle_pools()
     want = oatt.decode_attention_paged(case.q_store, kp, vp, case.tables, case.ctx, case.scale, case.kv_dtype,
                                        case.k_scale, case.v_scale, q_dtype=case.q_dtype, context_starts=c["starts"])
-    assert_close(out.cpu().numpy(), want, TOL[c["kv"]], str(c))
+    assert_close(out.cpu().numpy(), want, TOL[c["kv"]], f"{c} {kernel}")

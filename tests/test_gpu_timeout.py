@@ -17,10 +17,12 @@ from harness import TOL, Case, assert_close, to_torch
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_stage_times_out_and_the_context_survives(pa, cuda):
+@pytest.mark.parametrize("which", ["cta", "warp"])
+def test_stalled_stage_times_out_and_the_context_survives(pa, cuda, which):
     from paged_kv_cache_257_gb300 import _native, build
-    path = build.build_variant("test_stall", ["-DPA_TEST_EXTRA_TX=16"], ["decode_mma.cu"])
+    path = build.build_variant("test_stall", ["-DPA_TEST_EXTRA_TX=16"], ["decode_mma.cu", "decode_warp.cu"])
     stall = _native.load(path)
+    assert stall.pa_set_decode_kernel(_native.DECODE_KERNEL[which]) == 0
     # one sequence of one partition: a single CTA, so the waits run out once
     case = Case(batch=1, hq=8, hkv=1, d=128, bs=16, kv_dtype="bf16", q_dtype="bf16", ctx=[100], seed=71)
     kc, vc = case.gpu_pools(pa, cuda)

@@ -50,7 +50,8 @@ def _run(pa, cuda, case, starts, partition, out_dtype="f32"):
     ("bf16", "bf16", 16, 0), ("bf16", "bf16", 16, 256), ("bf16", "bf16", 16, 32), ("bf16", "bf16", 16, -1),
     ("f16", "f16", 8, 64), ("bf16", "bf16", 32, 128), ("fp8_e4m3", "bf16", 16, 512), ("fp8_e4m3", "bf16", 8, 32),
     ("f32", "f32", 16, 64)])
-def test_window_matches_oracle(pa, cuda, kv, q, bs, partition):
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_window_matches_oracle(pa, cuda, kernel, kv, q, bs, partition):
     ctx = [3000, 700, 129, 40, 16, 5, 77]
     # starts: deep into the context, none, at a chunk edge, one short of the
     # end, a whole first block, an empty window, and a start in the second
