@@ -204,7 +204,6 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     __syncthreads();
     const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
-    cs.convert_q(a.q_dtype == PA_BF16);
 
     const uint64_t policy = l2_evict_first_policy();
     BlockWindow win;   // this warp's chunks, in increasing order
@@ -248,6 +247,8 @@ decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
             ++issued;
         }
     }
+    // the query's widening waits for its loads: after the first copies are out
+    cs.convert_q(a.q_dtype == PA_BF16);
     int k = 0;
     for (int c = warp; c < n_chunks; ++k) {
         const int st = warp + kWarps * (k % S);

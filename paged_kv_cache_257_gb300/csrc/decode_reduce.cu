@@ -18,42 +18,87 @@ namespace pa {
 namespace {
 
 #ifndef PA_REDUCE_WARPS
-#define PA_REDUCE_WARPS 16
+#define PA_REDUCE_WARPS 8
 #endif
 constexpr int kWarps = PA_REDUCE_WARPS;
 constexpr int kThreads = kWarps * 32;
-constexpr int kUnroll = 8;   // partitions in flight per warp
+constexpr int kBatch = 8;   // partitions per warp and batch (two batches in flight)
 constexpr float kNegInf = -__builtin_huge_valf();
 
-// head_dim / 32 consecutive floats of a partial row: one vector load.
+// A batch of partials: kBatch (max, sum) pairs and, per lane, head_dim / 32
+// consecutive floats of each partial row (one coalesced row per partition).
 template <int N>
-struct Slice {
-    float v[N];
-    __device__ __forceinline__ void load(const float* p) {
-        if constexpr (N == 2) {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(p));
-            v[0] = t.x; v[1] = t.y;
-        } else {
+struct Batch {
+    float2 ml[kBatch];
+    float v[kBatch][N];
+    // partitions p0, p0 + step, ...; those at or past n_parts read as empty
+    __device__ __forceinline__ void load(const float2* mlrow, const float* orow, int p0, int step, int n_parts,
+                                         int D) {
 #pragma unroll
-            for (int i = 0; i < N; i += 4) {
-                const float4 t = __ldcg(reinterpret_cast<const float4*>(p + i));
-                v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+        for (int u = 0; u < kBatch; ++u) {
+            const int p = p0 + u * step;
+            if (p < n_parts) {
+                ml[u] = __ldcg(mlrow + p);
+                const float* src = orow + static_cast<int64_t>(p) * D;
+                if constexpr (N == 2) {
+                    const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+                    v[u][0] = t.x; v[u][1] = t.y;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < N; i += 4) {
+                        const float4 t = __ldcg(reinterpret_cast<const float4*>(src + i));
+                        v[u][i] = t.x; v[u][i + 1] = t.y; v[u][i + 2] = t.z; v[u][i + 3] = t.w;
+                    }
+                }
+            } else {
+                ml[u] = make_float2(kNegInf, 0.f);
+#pragma unroll
+                for (int i = 0; i < N; ++i) v[u][i] = 0.f;
             }
         }
     }
 };
 
-// One CTA per (query head, sequence).  Every warp takes the maximum of all
-// m_p itself, so no barrier precedes the sums; warp w then adds partitions
-// w, w+kWarps, ..., kUnroll of them in flight, lane j holding d = j*D/32 ..
-// (j+1)*D/32 - 1 of each partial row (one coalesced row per partition).  The
-// weights are the same in every lane, so each lane keeps the warp's weight
-// sum; the warps' sums meet in shared memory behind one barrier.
+// A running merge (max m, sum l, weighted rows acc) of partials.
+template <int N>
+struct Running {
+    float m = kNegInf, l = 0.f, acc[N];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.f;
+    }
+    __device__ __forceinline__ void add(const Batch<N>& b) {
+        float mb = kNegInf;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, b.ml[u].x);
+        if (mb == kNegInf) return;                      // only empty partitions
+        const float mn = fmaxf(m, mb);
+        const float s = m == kNegInf ? 0.f : exp2_approx(m - mn);
+        l *= s;
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] *= s;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const float w = b.ml[u].x == kNegInf ? 0.f : b.ml[u].y * exp2_approx(b.ml[u].x - mn);
+            l += w;
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[i] = fmaf(w, b.v[u][i], acc[i]);
+        }
+        m = mn;
+    }
+};
+
+// One CTA per (query head, sequence).  Warp w merges partitions w, w +
+// kWarps, w + 2 kWarps, ... online (a running maximum, its rows and sum
+// rescaled when it grows), kBatch partitions per batch, the next batch's
+// loads in flight while the current one is added, so the partials stream
+// in without a separate pass for the maximum.  The warps' running merges
+// meet in shared memory behind one barrier.
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArgs a) {
     constexpr int kVec = D / 32;
     __shared__ __align__(16) float s_acc[kWarps][D];
-    __shared__ float s_l[kWarps];
+    __shared__ float s_m[kWarps], s_l[kWarps];
     const int hq = blockIdx.x, seq = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();      // the partials come from the previous kernel in the stream
@@ -64,51 +109,41 @@ __global__ void __launch_bounds__(kThreads) decode_reduce_kernel(const DecodeArg
     const float2* ml = reinterpret_cast<const float2*>(a.part_ml + row * a.max_parts * 2);
     const float* po = a.part_o + row * a.max_parts * D + lane * kVec;
 
-    float M = kNegInf;
-#pragma unroll 4
-    for (int p = lane; p < n_parts; p += 32) M = fmaxf(M, __ldcg(ml + p).x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    Running<kVec> r;
+    r.init();
+    constexpr int kStride = kWarps * kBatch;   // partitions covered by one batch of every warp
+    Batch<kVec> b0, b1;
+    b0.load(ml, po, warp, kWarps, n_parts, D);
+    for (int p0 = warp; p0 < n_parts; p0 += 2 * kStride) {
+        b1.load(ml, po, p0 + kStride, kWarps, n_parts, D);
+        r.add(b0);
+        if (p0 + kStride >= n_parts) break;
+        b0.load(ml, po, p0 + 2 * kStride, kWarps, n_parts, D);
+        r.add(b1);
+    }
 
-    float acc[kVec];
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) acc[i] = 0.f;
-    float L = 0.f;
-    auto add = [&](const float2 mlp, const Slice<kVec>& o) {
-        const float w = mlp.x == kNegInf ? 0.f : mlp.y * exp2_approx(mlp.x - M);
-        L += w;
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) acc[i] = fmaf(w, o.v[i], acc[i]);
-    };
-    int p = warp;
-    for (; p + (kUnroll - 1) * kWarps < n_parts; p += kUnroll * kWarps) {
-        float2 mlp[kUnroll];
-        Slice<kVec> o[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            mlp[u] = __ldcg(ml + p + u * kWarps);
-            o[u].load(po + static_cast<int64_t>(p + u * kWarps) * D);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) add(mlp[u], o[u]);
+    for (int i = 0; i < kVec; ++i) s_acc[warp][lane * kVec + i] = r.acc[i];
+    if (lane == 0) {
+        s_m[warp] = r.m;
+        s_l[warp] = r.l;
     }
-    for (; p < n_parts; p += kWarps) {
-        Slice<kVec> o;
-        o.load(po + static_cast<int64_t>(p) * D);
-        add(__ldcg(ml + p), o);
-    }
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) s_acc[warp][lane * kVec + i] = acc[i];
-    if (lane == 0) s_l[warp] = L;
     __syncthreads();
-    float lt = 0.f;
+    float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) lt += s_l[w];
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w]);
+    float coef[kWarps], L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        coef[w] = s_m[w] == kNegInf ? 0.f : exp2_approx(s_m[w] - M);
+        L = fmaf(coef[w], s_l[w], L);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int d = threadIdx.x; d < D; d += kThreads) {
         float t = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += s_acc[w][d];
-        store_out(a.out, row * D + d, lt > 0.f ? t / lt : 0.f, a.out_dtype);
+        for (int w = 0; w < kWarps; ++w) t = fmaf(coef[w], s_acc[w][d], t);
+        store_out(a.out, row * D + d, t * inv, a.out_dtype);
     }
 }
 

@@ -77,15 +77,18 @@ decode_warp_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     const int nh = min(kHeadsPerCta, a.group - hg * kHeadsPerCta);
     const int32_t* bt_row = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
 
+    // The barriers need no inputs: set them up before anything is loaded.
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(smem_addr(full + i), 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+    }
     pdl_wait();      // inputs may come from the previous kernel in the stream
     pdl_trigger();
     WarpState<KV, C> cs;
     cs.init(lane);
     cs.reset();
-    if (lane == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_v);
-    }
     // The query, the context length and the partition's first 32 block ids
     // are loaded before any is waited on; the ids are a guess (blocks from
     // part * P / block_size), used only once the real partition start
@@ -103,13 +106,8 @@ decode_warp_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
     const int lead = sw.lead(part);   // positions of chunk 0 before the window
     const int n_chunks = tok1 > tok0 ? (tok1 - tok0 + kChunk - 1) / kChunk : 0;
 
-    if (lane == 0) {
-        for (int i = 0; i < S; ++i) mbar_init(smem_addr(full + i), 1);
-        fence_mbar_init();
-    }
     __syncwarp();
     const float sc = a.scale * 1.4426950408889634f * (kFp8 ? a.k_scale : 1.f);
-    cs.convert_q(a.q_dtype == PA_BF16);
 
     const uint64_t policy = l2_evict_first_policy();
     BlockWindow win;   // the item's chunks, in increasing order
@@ -133,6 +131,8 @@ decode_warp_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_cons
         issue(c, c);
         ++issued;
     }
+    // the query's widening waits for its loads: after the first copies are out
+    cs.convert_q(a.q_dtype == PA_BF16);
     int c = 0;
     for (; c < n_chunks; ++c) {
         const int st = c % S;
