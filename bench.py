@@ -291,19 +291,28 @@ class GpuWorkload:
         return n + 1 + self.merge_launches
 
 
-# DRAM bytes (read + write) of one decode_mma_kernel launch, from the ncu
-# captures summarised in profiles/decode_mma_<workload>.md.  They hold for the
-# kernel code they were taken on (the fingerprint of the files below, see
-# _code_fingerprint); after any change to that code traffic is reported as
-# null until a new capture is recorded here.
+# Counters of one launch of each workload's decode kernel (the warp-per-item
+# kernel for longctx_fp8, the CTA-per-item kernel for the others), from the
+# ncu captures summarised in profiles/: DRAM bytes read + written, and L2
+# read sectors / requests from the SMs' load unit (four 32-byte sectors per
+# request = whole 128-byte lines).  They hold for the kernel code they were
+# taken on (the fingerprint of the files below, see _code_fingerprint);
+# after any change to that code they are reported as null until a new
+# capture is recorded here.
 TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cache_257_gb300/csrc/decode_warp.cu",
                    "paged_kv_cache_257_gb300/csrc/mma_chunk.cuh", "paged_kv_cache_257_gb300/csrc/common.cuh",
                    "paged_kv_cache_257_gb300/csrc/decode.h", "paged_kv_cache_257_gb300/csrc/decode_epilogue.cuh",
                    "paged_kv_cache_257_gb300/csrc/window.cuh")
-NCU_TRAFFIC = {"c95e6201be2f6e43": {"gqa_bf16": 283_154_944 + 3_319_296,
-                                    "longctx_fp8": 1_074_071_296 + 7_793_152,
-                                    "mha_f16": 671_302_912 + 3_274_752,
-                                    "prefix_bf16": 72_584_704 + 1_070_592}}
+NCU_TRAFFIC = {"4cdd1064cf872625": {"longctx_fp8": 1_074_022_912 + 7_592_448,
+                                    "gqa_bf16": 283_151_360 + 3_324_672,
+                                    "mha_f16": 671_249_152 + 2_931_200,
+                                    "prefix_bf16": 72_584_192 + 835_072}}
+NCU_L2_SECTORS = {"4cdd1064cf872625": {"longctx_fp8": (42_150_239, 10_572_906),
+                                       "gqa_bf16": (11_124_599, 2_794_323),
+                                       "mha_f16": (26_238_115, 6_562_870),
+                                       "prefix_bf16": (9_794_822, 2_457_506)}}
+DECODE_KERNEL_OF = {"longctx_fp8": "decode_warp_kernel", "gqa_bf16": "decode_mma_kernel",
+                    "mha_f16": "decode_mma_kernel", "prefix_bf16": "decode_mma_kernel"}
 
 
 def _code_fingerprint(paths):
@@ -325,6 +334,11 @@ def _code_fingerprint(paths):
 
 def captured_traffic(workload):
     return NCU_TRAFFIC.get(_code_fingerprint(TRAFFIC_SOURCES), {}).get(workload)
+
+
+def captured_sectors_per_request(workload):
+    sr = NCU_L2_SECTORS.get(_code_fingerprint(TRAFFIC_SOURCES), {}).get(workload)
+    return None if sr is None else sr[0] / sr[1]
 
 
 def copy_blocks_timing(pa, torch, w, device, pairs=4096):
@@ -864,6 +878,7 @@ def workload_record(name, device, steps, warmup):
            "decode_us": dict(_stats_us(dec_ms), launch_avg=dec_launch_ms * 1e3, note=DECODE_US_NOTE),
            "kv_gbs": wk.kv_bytes / dec_s / 1e9,
            "frac": wk.kv_bytes / dec_s / 1e9 / peak, "traffic": captured_traffic(name),
+           "l2_sectors_per_request": captured_sectors_per_request(name),
            "kv_gbs_step": wk.kv_bytes / step_s / 1e9, "gpu_launches": launches,
            "l2": (f"{replicas} cache replicas rotated per step ({replicas * per / 2**20:.0f} MiB > L2)"
                   if replicas * per > L2_BYTES else f"KV ({per / 2**10:.0f} KiB) fits in L2: launch-bound")}
@@ -937,7 +952,9 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "paged decode (decode + split merge)", "achieved": achieved,
                      "duration": "decode_us.launch_avg: a CUDA-graph region of K decode launches / K",
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": captured_traffic(args.workload), "traffic_of": "one decode_mma_kernel launch (ncu)",
+                     "traffic": captured_traffic(args.workload),
+                     "traffic_of": f"one {DECODE_KERNEL_OF.get(args.workload, 'decode')} launch (ncu)",
+                     "l2_sectors_per_request": captured_sectors_per_request(args.workload),
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": wk.kv_bytes,
                      "nominal_peak_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

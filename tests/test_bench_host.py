@@ -41,6 +41,9 @@ def test_recorded_traffic_is_consistent():
         pytest.skip("no ncu capture recorded for the current kernel code")
     for w, kv in algorithmic.items():
         assert recorded[w] is not None and kv <= recorded[w] <= kv * 1.02, (w, recorded[w])
+        # the KV loads move whole 128-byte lines: four 32-byte sectors per L2 request
+        spr = bench.captured_sectors_per_request(w)
+        assert spr is not None and 3.9 <= spr <= 4.0, (w, spr)
 
 
 def test_oracle_sample_reads_the_workloads_own_tokens():
