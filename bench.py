@@ -754,7 +754,18 @@ def run_oracle(w_name, n_workers, calls=None, warmup=0, budget_s=None, window=0)
                                                           budget_s, barrier_, queue)) for i in range(n_workers)]
         for p in procs:
             p.start()
-        res = [queue.get(timeout=1800) for _ in procs]
+        res = []
+        t0 = time.perf_counter()
+        while len(res) < len(procs):
+            try:
+                res.append(queue.get(timeout=2.0))
+            except Exception:   # queue.Empty: a worker that died without a result ends the wait
+                dead = [p.exitcode for p in procs if p.exitcode not in (None, 0)]
+                if dead or time.perf_counter() - t0 > 1800:
+                    for p in procs:
+                        if p.is_alive():
+                            p.terminate()
+                    raise RuntimeError(f"oracle workers ended without results (exit codes {dead})")
         for p in procs:
             p.join(timeout=60)
     finally:
