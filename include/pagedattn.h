@@ -310,8 +310,9 @@ int32_t pa_get_decode_deterministic(void);
  * warps.
  *   PA_DECODE_KERNEL_AUTO (default): the library picks per call: one warp
  *     per work item when partitions are at least 512 tokens and the grid
- *     holds work items for at least two thirds of the GPU's warp slots (20
- *     per SM), else one CTA of four warps per work item.
+ *     (every sequence counted at max_blocks_per_seq * block_size tokens)
+ *     holds at least two work items per warp slot of the GPU (20 per SM),
+ *     else one CTA of four warps per work item.
  *   PA_DECODE_KERNEL_CTA: always a CTA of four warps per work item (an
  *     item's chunks split among the warps, whose states are merged).
  *   PA_DECODE_KERNEL_WARP: always one warp per work item.

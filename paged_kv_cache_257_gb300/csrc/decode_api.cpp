@@ -142,19 +142,21 @@ size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q
 // Kernel choice for the tensor-core path.  One warp streams an item about
 // four times slower than a CTA of four warps, but it pays no pipeline fill
 // of its own while other warps stream and no cross-warp merge; that wins
-// when the items are long (partitions of 512 tokens or more) and there are
-// enough of them to give most warp slots of the GPU one.  Measured on GB300
-// (decode us, CTA kernel against warp kernel): 128k-token FP8 contexts in
-// 512-token partitions (8192 items) 175 / 165; their last 32760 tokens
-// (2048 items) 56.5 / 51.4; a Llama-3-8B ragged batch in 512-token
-// partitions (2048 at most) 49.0 / 48.5.  The item count here is the
-// grid's upper bound (every sequence at the table's capacity).
+// when the items are long (partitions of 512 tokens or more) and many.  The
+// host does not know the context lengths (or window starts) here, so the
+// count is the grid's upper bound, every sequence at the table's capacity,
+// and it must cover two waves of warp slots.  Measured on GB300 (decode us,
+// CTA kernel / warp kernel, upper bound on items): 128k-token FP8 contexts
+// in 512-token partitions 175 / 165 (8192); their last 32760 tokens
+// 56.5 / 51.4 (8192, 2048 real); a Llama-3-8B ragged batch in 512-token
+// partitions 49.0 / 48.5 (2048), the same batch's last 1000 tokens
+// 24.9 / 30.8 (2048, about 512 real).
 bool warp_path_preferred(const DecodeArgs& a) {
     if (a.partition_size < 512) return false;
     const int64_t n_hg = (a.group + kHeadsPerCta - 1) / kHeadsPerCta;
     const int64_t items = static_cast<int64_t>(a.max_parts) * a.num_kv_heads * n_hg * a.batch;
     const int64_t slots = static_cast<int64_t>(PA_DECODE_WARP_MIN_CTAS) * std::max(sm_count(), 1);
-    return 3 * items >= 2 * slots;
+    return items >= 2 * slots;
 }
 
 }  // namespace pa

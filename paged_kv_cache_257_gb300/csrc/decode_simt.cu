@@ -5,9 +5,10 @@
 // (partition, KV head, sequence) and up to 8 query heads; 4 warps take
 // 16-token chunks in turn.  A warp walks its chunk token by token: each lane
 // holds head_dim/32 consecutive elements of the token's K and V rows (one
-// coalesced row read per warp), the dot product with every query head is a
-// warp reduction, and the online softmax (running max, running sum, rescaled
-// output) is updated in float32.  Only tokens below the context length are
+// coalesced row read per warp; the rows of 16 / (head_dim/32) tokens are
+// loaded together before the first is used), the dot product with every
+// query head is a warp reduction, and the online softmax (running max,
+// running sum, rescaled output) is updated in float32, token by token.  Only tokens below the context length are
 // read.  dev.to "Why LLMs Run Out of VRAM...", section 4 "The PagedAttention
 // CUDA Kernel" (block-table lookup inside the attention loop) and section 1
 // (the attention formula).
@@ -39,6 +40,7 @@ __device__ __forceinline__ float load_q(const void* q, int64_t i, pa_dtype t) {
 template <pa_dtype KV, int D>
 __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeArgs a) {
     constexpr int E = D / 32;  // elements per lane
+    constexpr int kTok = 16 / E;   // tokens whose rows are loaded together (2 to 8)
     extern __shared__ float msm[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seq = blockIdx.z;
@@ -79,35 +81,49 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(const DecodeAr
     const int32_t* bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
     for (int c0 = tok0 + warp * kChunk; c0 < tok1; c0 += kWarps * kChunk) {
         const int c1 = min(tok1, c0 + kChunk);
-        for (int t = max(c0, sw.start); t < c1; ++t) {
-            const int pb = __ldg(bt + t / bs);
-            if (pb < 0 || pb >= a.num_blocks) {
-                if (lane == 0) raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
-                continue;
+        const int tl = max(c0, sw.start);
+        // the chunk's block ids, one per lane (token c0 + lane), then its K
+        // and V rows kTok tokens at a time, all loads of a group in flight
+        // before the first is used
+        const int my_pb = lane < c1 - c0 ? __ldg(bt + (c0 + lane) / bs) : 0;
+        for (int t0 = c0; t0 < c1; t0 += kTok) {
+            float kx[kTok][E], vx[kTok][E];
+            bool ok[kTok];
+#pragma unroll
+            for (int u = 0; u < kTok; ++u) {
+                const int t = t0 + u;
+                const int pb = __shfl_sync(0xffffffffu, my_pb, (t - c0) & 31);
+                const bool in = t >= tl && t < c1;
+                ok[u] = in && pb >= 0 && pb < a.num_blocks;
+                if (in && !ok[u] && lane == 0) raise_flag(a.status, PA_DEVFLAG_BLOCK_RANGE);
+                const int64_t row =
+                    ok[u] ? ((static_cast<int64_t>(pb) * a.num_kv_heads + kvh) * bs + t % bs) * D + lane * E : 0;
+#pragma unroll
+                for (int i = 0; i < E; ++i) {
+                    kx[u][i] = ok[u] ? to_float<KV>(a.k_cache, row + i) * ks : 0.f;
+                    vx[u][i] = ok[u] ? to_float<KV>(a.v_cache, row + i) * vs : 0.f;
+                }
             }
-            const int64_t row = ((static_cast<int64_t>(pb) * a.num_kv_heads + kvh) * bs + t % bs) * D + lane * E;
-            float kx[E], vx[E];
 #pragma unroll
-            for (int i = 0; i < E; ++i) {
-                kx[i] = to_float<KV>(a.k_cache, row + i) * ks;
-                vx[i] = to_float<KV>(a.v_cache, row + i) * vs;
-            }
+            for (int u = 0; u < kTok; ++u) {
+                if (!ok[u]) continue;
 #pragma unroll
-            for (int h = 0; h < kHeadsPerCta; ++h) {
-                if (h >= nh) break;
-                float dot = 0.f;
+                for (int h = 0; h < kHeadsPerCta; ++h) {
+                    if (h >= nh) break;
+                    float dot = 0.f;
 #pragma unroll
-                for (int i = 0; i < E; ++i) dot = fmaf(qv[h][i], kx[i], dot);
+                    for (int i = 0; i < E; ++i) dot = fmaf(qv[h][i], kx[u][i], dot);
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-                const float x = dot * sc;
-                const float mn = fmaxf(m[h], x);
-                const float al = exp2_approx(m[h] - mn);
-                const float p = exp2_approx(x - mn);
-                l[h] = l[h] * al + p;
+                    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                    const float x = dot * sc;
+                    const float mn = fmaxf(m[h], x);
+                    const float al = exp2_approx(m[h] - mn);
+                    const float p = exp2_approx(x - mn);
+                    l[h] = l[h] * al + p;
 #pragma unroll
-                for (int i = 0; i < E; ++i) acc[h][i] = fmaf(p, vx[i], acc[h][i] * al);
-                m[h] = mn;
+                    for (int i = 0; i < E; ++i) acc[h][i] = fmaf(p, vx[u][i], acc[h][i] * al);
+                    m[h] = mn;
+                }
             }
         }
     }
