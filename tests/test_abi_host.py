@@ -47,6 +47,22 @@ def test_decode_deterministic_setting_round_trips(pa):
         pa.set_decode_deterministic(prev)
 
 
+def test_decode_kernel_setting_round_trips_and_rejects_unknown_values(pa):
+    from paged_kv_cache_257_gb300 import _native
+    lib = _native.lib()
+    prev = pa.decode_kernel()
+    try:
+        assert pa.set_decode_kernel("warp") == prev
+        assert pa.decode_kernel() == "warp" and lib.pa_get_decode_kernel() == 2
+        assert pa.set_decode_kernel("cta") == "warp"
+        assert lib.pa_set_decode_kernel(7) == 1                  # PA_ERR_INVALID, setting unchanged
+        assert lib.pa_set_decode_kernel(-1) == 1
+        assert pa.decode_kernel() == "cta"
+        assert pa.set_decode_kernel("auto") == "cta"
+    finally:
+        pa.set_decode_kernel(prev)
+
+
 def test_version_and_status_strings(pa):
     from paged_kv_cache_257_gb300 import _native
     assert "sm_103a" in pa.version()
