@@ -177,8 +177,10 @@ int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int3
  * size partitions; this models a call as waves of work items (one per
  * partition, sequence and group of up to 8 query heads) over the resident
  * CTAs, each wave as long as its longest item plus a fixed per-item cost,
- * and returns the candidate (the whole context, 8192 ... 256 tokens) with
- * the least modelled time.  Pass the result as pa_decode_attention's
+ * and returns the candidate (the whole context, the powers of two from 8192
+ * down to 256 tokens, and the multiples of 128 between 1024 and 4096 whose
+ * items fit one wave) with the least modelled time; ties keep the power of
+ * two and the larger size.  Pass the result as pa_decode_attention's
  * partition_size with the same cache, batch, num_q_heads and
  * max_blocks_per_seq.
  *   host_context_lens  host [batch] int32 (null: every sequence full)

@@ -285,14 +285,25 @@ def test_plan_partition_follows_the_wave_model(pa):
     assert pa.plan_partition(gqa, 32, 32, 256, None, 152) == 512
     fp8 = pa.CacheDesc(32768, 16, 8, 128, "fp8_e4m3", 0.01, 0.01)
     # 4 x 131072 tokens, 64 query heads (one group of 8 per KV head): 2048 -> 3 x 2240
-    # beats 1024 -> 6 x 1216, 512 -> 11 x 704 and 4096 -> 2 x 4288
+    # beats 1024 -> 6 x 1216, 512 -> 11 x 704 and 4096 -> 2 x 4288; the finer grid's
+    # 2816 (47 x 32 = 1504 items, 2 x (2800 + 192) = 5984) spans two waves and is not taken
     assert pa.plan_partition(fp8, 4, 64, 8192, [131072] * 4, 152) == 2048
+    # a batch of long items that leaves a third of the CTA slots idle when whole:
+    # 64 sequences of 2049..2561 tokens (8 KV heads, whole = 2576): 512 items,
+    # 1 x (2561 + 192); at 2304 the 32 longest split in two (their shares <= 1296):
+    # (32 + 2 x 32) x 8 = 768 > 760 slots, 2 waves; at 2432 the 16 longest split:
+    # 640 items, 1 x (2432 + 192) = 2624, the least
+    lens = [2049 + (512 * i) // 63 for i in range(64)]
+    assert pa.plan_partition(gqa, 64, 32, 161, lens, 152) == 2432
     # a ragged batch plans from its real lengths: one long sequence among short
     # ones is cut finest, as all its pieces still fit one wave:
     # 256 -> (16 + 31 x 2) x 8 = 624 items, 1 x (256 + 192) beats 512 -> 1 x 704
     assert pa.plan_partition(gqa, 32, 32, 256, [4096] + [300] * 31, 152) == 256
-    # ... and not when the batch is long as a whole (the full case above gives 512)
-    assert pa.plan_partition(gqa, 32, 32, 256, [4096] * 31 + [300], 152) == 512
+    # ... and a long batch takes the finer grid when it fills one wave: 31 x 4096 + 300
+    # at 1920 -> 3 shares of 1376 each, (31 x 3 + 1) x 8 = 752 items, 1 x (1376 + 192) =
+    # 1568, beats 512 -> 1992 items, 3 x 704 = 2112 (32 x 4096 at 1920 needs 768 items,
+    # two waves: 3136, so the full case above keeps 512)
+    assert pa.plan_partition(gqa, 32, 32, 256, [4096] * 31 + [300], 152) == 1920
     bs32 = pa.CacheDesc(4096, 32, 8, 128, "bf16", 1.0, 1.0)
     assert pa.plan_partition(bs32, 32, 32, 128, [4096] * 32, 152) % 32 == 0
 
