@@ -306,11 +306,11 @@ TRAFFIC_SOURCES = ("paged_kv_cache_257_gb300/csrc/decode_mma.cu", "paged_kv_cach
 NCU_TRAFFIC = {"4cdd1064cf872625": {"longctx_fp8": 1_074_022_912 + 7_592_448,
                                     "gqa_bf16": 283_151_360 + 3_324_672,
                                     "mha_f16": 671_249_152 + 2_931_200,
-                                    "prefix_bf16": 72_584_192 + 835_072}}
+                                    "prefix_bf16": 72_591_104 + 977_920}}
 NCU_L2_SECTORS = {"4cdd1064cf872625": {"longctx_fp8": (42_150_239, 10_572_906),
                                        "gqa_bf16": (11_124_599, 2_794_323),
                                        "mha_f16": (26_238_115, 6_562_870),
-                                       "prefix_bf16": (9_794_822, 2_457_506)}}
+                                       "prefix_bf16": (14_301_736, 3_591_418)}}
 DECODE_KERNEL_OF = {"longctx_fp8": "decode_warp_kernel", "gqa_bf16": "decode_mma_kernel",
                     "mha_f16": "decode_mma_kernel", "prefix_bf16": "decode_mma_kernel"}
 
