@@ -44,11 +44,21 @@ def _expected(pa, case, kc, vc, qt, bt, cl, partition):
     return case.oracle_out(kp, vp), ordinary.cpu().numpy()
 
 
-@pytest.mark.parametrize("kv,q,partition", [("bf16", "bf16", 256),      # few partitions: fused merge
-                                             ("bf16", "bf16", 32),       # many partitions: merge kernel
-                                             ("fp8_e4m3", "bf16", 512),
-                                             ("f32", "f32", 64)])        # CUDA-core kernel
-def test_noalloc_matches_the_oracle_and_the_ordinary_entry_point_twice(pa, cuda, kv, q, partition):
+@pytest.mark.parametrize("kv,q,partition,kernel", [("bf16", "bf16", 256, "auto"),    # few partitions: fused merge
+                                                    ("bf16", "bf16", 32, "auto"),     # many partitions: merge kernel
+                                                    ("fp8_e4m3", "bf16", 512, "auto"),
+                                                    ("fp8_e4m3", "bf16", 512, "warp"),  # one warp per work item
+                                                    ("bf16", "bf16", 32, "warp"),
+                                                    ("f32", "f32", 64, "auto")])      # CUDA-core kernel
+def test_noalloc_matches_the_oracle_and_the_ordinary_entry_point_twice(pa, cuda, kv, q, partition, kernel):
+    prev = pa.set_decode_kernel(kernel)
+    try:
+        _noalloc_against_oracle(pa, cuda, kv, q, partition)
+    finally:
+        pa.set_decode_kernel(prev)
+
+
+def _noalloc_against_oracle(pa, cuda, kv, q, partition):
     case = Case(batch=4, hq=16, hkv=4, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[3000, 700, 1, 129], seed=21)
     kc, vc, qt, bt, cl = _inputs(pa, cuda, case)
     oracle, ordinary = _expected(pa, case, kc, vc, qt, bt, cl, partition)
