@@ -6,10 +6,11 @@ These tests capture the library's calls (no allocation or synchronisation
 happens inside them when the output and workspace are given) and check
 the replays:
 - against the same calls run eagerly on the same inputs: bit for bit in
-  the deterministic schedule; in the default one, with 16-bit caches, an
-  item's last chunks go to whichever warp is free, so a warp's softmax
-  reference and sums can differ between runs at the level of bf16 rounding
-  of the probabilities (FP8 keeps a fixed schedule: bit for bit);
+  the deterministic schedule; in the default one, with 16-bit caches, the
+  CTA-per-item kernel gives an item's last chunks to whichever warp is free,
+  so a warp's softmax reference and sums can differ between runs at the
+  level of bf16 rounding of the probabilities (FP8 and the warp-per-item
+  kernel keep fixed schedules: bit for bit);
 - against the oracle, within the dtype's tolerance.
 """
 
@@ -39,8 +40,9 @@ def schedule(pa, request):
     pa.set_decode_deterministic(prev)
 
 
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
 @pytest.mark.parametrize("kv,q,partition", [("bf16", "bf16", 256), ("fp8_e4m3", "bf16", 64), ("f16", "f16", -1)])
-def test_decode_replays_match_eager_and_oracle(pa, cuda, kv, q, partition, schedule):
+def test_decode_replays_match_eager_and_oracle(pa, cuda, kernel, kv, q, partition, schedule):
     # partition 256: the fused merge; 64: 47 partitions, the merge kernel; -1: unsplit
     case = Case(batch=5, hq=16, hkv=4, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[3000, 17, 700, 1, 1234], seed=71)
     desc = case.desc(pa)
@@ -76,7 +78,7 @@ def test_decode_replays_match_eager_and_oracle(pa, cuda, kv, q, partition, sched
         got = out.clone()
         step()                                       # the same calls, eagerly
         torch.cuda.synchronize()
-        if schedule or kv == "fp8_e4m3":             # fixed chunk order: bit for bit
+        if schedule or kv == "fp8_e4m3" or kernel == "warp":   # fixed chunk order: bit for bit
             assert torch.equal(got, out), f"round {rnd}: graph replay differs from the eager call"
         else:                                        # bf16 rounding of the probabilities
             assert_close(got.cpu().numpy(), out.cpu().numpy().astype(np.float64), 2e-3, f"round {rnd} vs eager")
