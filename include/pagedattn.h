@@ -166,12 +166,6 @@ pa_status pa_copy_blocks(const pa_cache_desc* cache, void* k_cache, void* v_cach
 int32_t pa_decode_partition_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                  int32_t max_blocks_per_seq, int32_t requested);
 
-/* Bytes of device workspace pa_decode_attention needs for these arguments:
- * when contexts are split, the merge counters and the partial softmax state
- * of the partitions; 0 when every sequence fits one partition (or for
- * invalid input).  The workspace must be zero-filled before its first use;
- * every completed call leaves its counters at zero again, so one zeroed
- * buffer serves any sequence of calls that are not concurrent. */
 /* Partition size for a batch whose context lengths the host knows (a
  * serving loop knows them: it built the block tables).  The pages do not
  * size partitions; this models a call as waves of work items (one per
@@ -190,6 +184,12 @@ int32_t pa_decode_plan_partition(const pa_cache_desc* cache, int32_t batch, int3
                                  int32_t max_blocks_per_seq, const int32_t* host_context_lens,
                                  int32_t num_sms);
 
+/* Bytes of device workspace pa_decode_attention needs for these arguments:
+ * when contexts are split, the merge counters and the partial softmax state
+ * of the partitions; 0 when every sequence fits one partition (or for
+ * invalid input).  The workspace must be zero-filled before its first use;
+ * every completed call leaves its counters at zero again, so one zeroed
+ * buffer serves any sequence of calls that are not concurrent. */
 size_t pa_decode_workspace_size(const pa_cache_desc* cache, int32_t batch, int32_t num_q_heads,
                                 int32_t max_blocks_per_seq, int32_t partition_size);
 
