@@ -217,6 +217,16 @@ def test_decode_rejects_bad_arguments_before_any_launch(pa):
     assert _call_decode(pa, pa.CacheDesc(1024, 16, 8, 128, "fp8_e4m3", 0.0, 1.0)) == 1
 
 
+def test_decode_rejects_grids_beyond_the_launch_limits(pa):
+    """Limits checked before any launch: 65535 sequences (the grid's z
+    extent), 32768 partitions per sequence, and tables of 2^31 tokens."""
+    d = pa.CacheDesc(1024, 16, 8, 128, "bf16")
+    assert _call_decode(pa, d, batch=65536, part=-1) == 4
+    assert _call_decode(pa, d, max_blocks=32769, part=16, ws=8192, ws_bytes=1 << 40) == 4   # 32769 partitions
+    assert _call_decode(pa, d, max_blocks=1 << 27, part=-1) == 4                          # 2^31 tokens
+    assert pa.partition_size(d, 4, 32, 1 << 27, -1) == -1
+
+
 def test_noalloc_rejects_null_pointers_and_oversized_problems_on_the_host(pa):
     """The allocation-free entry point answers before any CUDA call: a null
     input or output of a split call is PA_ERR_INVALID, a workspace beyond
