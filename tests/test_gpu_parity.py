@@ -46,6 +46,17 @@ def test_tensor_core_path_ragged(pa, cuda, kernel, kv, q, hq, hkv):
     assert_close(got, expect, TOL[kv], f"{kv} G={hq // hkv} {kernel}")
 
 
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (10, 2), (24, 2), (32, 1), (64, 1)])
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp8_e4m3", "f16")])
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_group_sizes_beyond_one_cta(pa, cuda, kernel, kv, q, hq, hkv):
+    """G = 3, 5, 12, 32, 64: groups of fewer than 8 heads, and groups split
+    over several 8-head work items (12 = 8 + 4)."""
+    case = Case(batch=4, hq=hq, hkv=hkv, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[1, 300, 1000, 77], seed=hq)
+    got, expect = _run(pa, cuda, case, partition=256)
+    assert_close(got, expect, TOL[kv], f"{kv} G={hq // hkv} {kernel}")
+
+
 @pytest.mark.parametrize("partition", [-1, 16, 64, 256, 512, 0])
 @pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp8_e4m3", "bf16"), ("f32", "f32")])
 @pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
