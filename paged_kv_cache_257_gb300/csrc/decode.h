@@ -42,8 +42,9 @@ constexpr int kHeadsPerCta = 8;
 #define PA_DECODE_MIN_CTAS 5
 #endif
 
-// CTAs (one warp each) of the warp-per-item decode kernel resident per SM
-// (its register budget is sized for this many).
+// CTAs (one warp each) of the warp-per-item decode kernel per SM that its
+// register budget is sized for: the residency with FP8 caches (shared
+// memory holds 11 with 16-bit caches).
 #ifndef PA_DECODE_WARP_MIN_CTAS
 #define PA_DECODE_WARP_MIN_CTAS 20
 #endif

@@ -158,7 +158,8 @@ size_t decode_counter_bytes(const pa_cache_desc* c, int32_t batch, int32_t num_q
 // when the items are long (partitions of 512 tokens or more) and many.  The
 // host does not know the context lengths (or window starts) here, so the
 // count is the grid's upper bound, every sequence at the table's capacity,
-// and it must cover two waves of warp slots.  Measured on GB300 (decode us,
+// and it must cover two waves of warp slots (counted at 20 per SM, the FP8
+// residency, for every cache type).  Measured on GB300 (decode us,
 // CTA kernel / warp kernel, upper bound on items): 128k-token FP8 contexts
 // in 512-token partitions 175 / 165 (8192); their last 32760 tokens
 // 56.5 / 51.4 (8192, 2048 real); a Llama-3-8B ragged batch in 512-token

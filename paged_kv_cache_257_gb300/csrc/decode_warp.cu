@@ -16,8 +16,9 @@
 // (mma.sync S^T = K Q^T, online softmax, O^T += V^T P^T).  Its softmax state
 // is the item's result, so there is no cross-warp merge, no CTA barrier and
 // no merge buffer: an item ends with the warp's rows normalised in
-// registers, staged in its ring and written out, while about 20 such warps
-// per SM keep their copies in flight.  When items are long and many (a
+// registers, staged in its ring and written out, while up to 20 such warps
+// per SM keep their copies in flight (20 with FP8 caches; with 16-bit
+// caches the two 8 KB stages per warp let shared memory hold 11).  When items are long and many (a
 // 128k-token FP8 context in 512-token partitions gives 8192 of 32 chunks), a
 // CTA of four warps spends a third of its life filling its pipeline and
 // merging its warps; independent warps remove the merge and let every other
@@ -55,7 +56,9 @@ struct WarpCfg : TileCfg<KV, BS> {
     static constexpr int kSmemBytes = 1024 + kDataBytes + S * 8;         // + one full barrier per stage
 };
 
-// One warp per CTA and per item; PA_DECODE_WARP_MIN_CTAS resident per SM.
+// One warp per CTA and per item; registers sized for PA_DECODE_WARP_MIN_CTAS
+// resident per SM (shared memory allows that many with FP8 caches, 11 with
+// 16-bit ones).
 template <pa_dtype KV, int BS, int S>
 __global__ void __launch_bounds__(32, PA_DECODE_WARP_MIN_CTAS)
 decode_warp_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
