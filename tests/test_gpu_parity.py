@@ -4,6 +4,8 @@ attention outputs within the tolerance of the cache type:
 1e-5 (float32 cache), 1e-2 (16-bit cache), 3e-2 (FP8 cache, oracle on the same
 dequantised values), with float32 outputs."""
 
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -55,6 +57,28 @@ def test_group_sizes_beyond_one_cta(pa, cuda, kernel, kv, q, hq, hkv):
     case = Case(batch=4, hq=hq, hkv=hkv, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[1, 300, 1000, 77], seed=hq)
     got, expect = _run(pa, cuda, case, partition=256)
     assert_close(got, expect, TOL[kv], f"{kv} G={hq // hkv} {kernel}")
+
+
+@pytest.mark.parametrize("scale", [0.0, 1e-3, 1.0, 30.0])
+@pytest.mark.parametrize("kv,q", [("bf16", "bf16"), ("fp8_e4m3", "bf16"), ("f32", "f32")])
+@pytest.mark.parametrize("kernel", ["cta", "warp"], indirect=True)
+def test_softmax_scale_extremes(pa, cuda, kernel, kv, q, scale):
+    """Scale 0 (every token weighs the same: the mean of V), a tiny scale,
+    and large ones, where the scores of one chunk jump far past the running
+    maximum (the rescale path) and the weights approach one-hot."""
+    case = Case(batch=3, hq=8, hkv=2, d=128, bs=16, kv_dtype=kv, q_dtype=q, ctx=[700, 33, 2000], seed=23)
+    case.scale = scale
+    got, expect = _run(pa, cuda, case, partition=256)
+    # float32 caches: the scores' float32 rounding grows with the scale
+    # (about |q||k| x 2^-24 per dot product, times the scale, becomes the
+    # weights' relative error); the 1e-5 bar holds at 1/sqrt(D) ~ 0.088.
+    tol = TOL[kv] * max(1.0, scale * math.sqrt(128)) if kv == "f32" else TOL[kv]
+    assert_close(got, expect, tol, f"{kv} scale={scale} {kernel}")
+    if scale == 0.0:   # the plain mean of the dequantised values
+        kp, vp = case.oracle_pools()
+        from oracle import cache as ocache
+        v = numerics.to_f64(ocache.gather_logical(vp, case.tables[1], 33, 0), kv, case.v_scale)
+        np.testing.assert_allclose(expect[1, 0], v[:, 0].mean(axis=0), rtol=0, atol=1e-12)
 
 
 @pytest.mark.parametrize("partition", [-1, 16, 64, 256, 512, 0])
